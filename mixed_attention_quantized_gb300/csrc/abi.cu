@@ -1,0 +1,403 @@
+// abi.cu -- host side of the C ABI: validation, the ForwardBatch planner and
+// the launches.  See include/mixattn.h for the contract of every entry point.
+//
+// Page "自研RDNA高併發推論引擎 以AI Max+ 395為範例": §1 (chunk rows and decode
+// rows share one ForwardBatch and one attention kernel; a prompt is fed one
+// bounded chunk per round) and §2 (blocked Q8 / 4-bit KV modes).
+#include <cuda_runtime.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+
+namespace mixattn {
+
+__device__ unsigned int g_device_error = 0u;
+
+namespace {
+
+// Address of this device's error word (kernels receive it as an argument).
+unsigned int* error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  static std::mutex mu;
+  static unsigned int* ptrs[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned int*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_fmt(int f) { return f == MIXATTN_KV_F16 || f == MIXATTN_KV_Q8_0 || f == MIXATTN_KV_Q4_0; }
+
+// Dimensions and formats only (no pointers).
+int check_cache_dims(const mixattn_kv_cache* c) {
+  if (!c) return MIXATTN_ERR_INVALID_ARG;
+  if (c->num_pages <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0) return MIXATTN_ERR_INVALID_ARG;
+  if (c->page_size != kPage) return MIXATTN_ERR_UNSUPPORTED;
+  if (c->head_dim % kBlock != 0) return MIXATTN_ERR_INVALID_ARG;
+  if (c->head_dim != 64 && c->head_dim != 128) return MIXATTN_ERR_UNSUPPORTED;
+  if (!valid_fmt(c->k_fmt) || !valid_fmt(c->v_fmt)) return MIXATTN_ERR_INVALID_ARG;
+  const bool kf = c->k_fmt == MIXATTN_KV_F16, vf = c->v_fmt == MIXATTN_KV_F16;
+  if (kf != vf) return MIXATTN_ERR_UNSUPPORTED;  // fp16 pairs only with fp16
+  if ((int64_t)c->num_pages * kPage > INT32_MAX) return MIXATTN_ERR_INVALID_ARG;
+  return MIXATTN_OK;
+}
+
+int check_cache(const mixattn_kv_cache* c) {
+  int st = check_cache_dims(c);
+  if (st != MIXATTN_OK) return st;
+  if (!c->k_quant || !c->v_quant) return MIXATTN_ERR_INVALID_ARG;
+  if (!aligned(c->k_quant, 256) || !aligned(c->v_quant, 256)) return MIXATTN_ERR_INVALID_ARG;
+  if (c->k_fmt != MIXATTN_KV_F16 && (!c->k_scale || !aligned(c->k_scale, 256))) return MIXATTN_ERR_INVALID_ARG;
+  if (c->v_fmt != MIXATTN_KV_F16 && (!c->v_scale || !aligned(c->v_scale, 256))) return MIXATTN_ERR_INVALID_ARG;
+  return MIXATTN_OK;
+}
+
+cudaError_t dispatch_attention(int k_fmt, int v_fmt, int head_dim, const AttnParams& p, unsigned int* err,
+                               cudaStream_t s) {
+  if (k_fmt == MIXATTN_KV_F16) return launch_attention_f16_f16(head_dim, p, err, s);
+  if (k_fmt == MIXATTN_KV_Q8_0 && v_fmt == MIXATTN_KV_Q8_0) return launch_attention_q8_q8(head_dim, p, err, s);
+  if (k_fmt == MIXATTN_KV_Q4_0 && v_fmt == MIXATTN_KV_Q4_0) return launch_attention_q4_q4(head_dim, p, err, s);
+  if (k_fmt == MIXATTN_KV_Q8_0) return launch_attention_q8_q4(head_dim, p, err, s);
+  return launch_attention_q4_q8(head_dim, p, err, s);
+}
+
+// The tiling of one batch: the image uploaded to the workspace plus counts.
+struct Tiling {
+  std::vector<uint8_t> image;  // [rows | tiles | counters], from WorkspaceLayout::rows
+  int32_t total_q = 0, n_chunk = 0, n_decode = 0;
+  WorkspaceLayout L{};
+};
+
+int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* kinds, const int32_t* seq,
+                 const int32_t* off, int max_pages, Tiling* out) {
+  if (n_rows <= 0 || !kinds || !seq || !off || max_pages <= 0) return MIXATTN_ERR_INVALID_ARG;
+  if (hq <= 0 || hq % c.num_kv_heads != 0) return MIXATTN_ERR_INVALID_ARG;
+  const int G = hq / c.num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return MIXATTN_ERR_UNSUPPORTED;
+  const int hkv = c.num_kv_heads;
+  const int T = kChunkM / G;  // query tokens per chunk tile
+
+  std::vector<RowInfo> rows(n_rows);
+  struct Chunk {
+    TileDesc t;
+    int64_t cost;
+  };
+  std::vector<Chunk> chunks;
+  std::vector<TileDesc> decodes;
+  int64_t total_q = 0;
+  for (int r = 0; r < n_rows; ++r) {
+    const int64_t s = seq[r], o = off[r];
+    if (kinds[r] == MIXATTN_ROW_DECODE) {
+      if (s < 1 || o != s - 1) return MIXATTN_ERR_INVALID_ARG;
+    } else if (kinds[r] == MIXATTN_ROW_CHUNK) {
+      if (o < 0 || o >= s) return MIXATTN_ERR_INVALID_ARG;
+    } else {
+      return MIXATTN_ERR_INVALID_ARG;
+    }
+    const int64_t n_pages = (s + kPage - 1) / kPage;
+    if (n_pages > max_pages) return MIXATTN_ERR_INVALID_ARG;
+    if (n_pages > c.num_pages) return MIXATTN_ERR_INVALID_ARG;
+    rows[r].q_start = (int32_t)total_q;
+    rows[r].seq_len = (int32_t)s;
+    rows[r].q_offset = (int32_t)o;
+    rows[r].n_splits = 0;
+    const int64_t nq = s - o;
+    if (kinds[r] == MIXATTN_ROW_CHUNK) {
+      for (int g = 0; g < hkv; ++g) {
+        for (int64_t b = 0; b < nq; b += T) {
+          Chunk ch;
+          ch.t.row = r;
+          ch.t.kvh = g;
+          ch.t.begin = (int32_t)b;
+          ch.t.count = (int32_t)std::min<int64_t>(T, nq - b);
+          const int64_t key_end = std::min<int64_t>(s, o + b + ch.t.count);
+          ch.cost = (key_end + kChunkN - 1) / kChunkN;
+          chunks.push_back(ch);
+        }
+      }
+    } else {
+      const int pps = decode_pages_per_split((int)n_pages);
+      const int ns = (int)((n_pages + pps - 1) / pps);
+      rows[r].n_splits = ns;
+      for (int g = 0; g < hkv; ++g) {
+        for (int sp = 0; sp < ns; ++sp) {
+          TileDesc t;
+          t.row = r;
+          t.kvh = g;
+          t.begin = sp * pps;
+          t.count = (int32_t)std::min<int64_t>(pps, n_pages - (int64_t)sp * pps);
+          decodes.push_back(t);
+        }
+      }
+    }
+    total_q += nq;
+    if (total_q > INT32_MAX / std::max(hq, 1)) return MIXATTN_ERR_INVALID_ARG;
+  }
+  // heaviest chunk tiles first (they set the length of the launch)
+  std::stable_sort(chunks.begin(), chunks.end(), [](const Chunk& a, const Chunk& b) { return a.cost > b.cost; });
+  const int64_t n_tiles = (int64_t)chunks.size() + (int64_t)decodes.size();
+  if (n_tiles > INT32_MAX / 2) return MIXATTN_ERR_INVALID_ARG;
+
+  Tiling& T2 = *out;
+  T2.total_q = (int32_t)total_q;
+  T2.n_chunk = (int32_t)chunks.size();
+  T2.n_decode = (int32_t)decodes.size();
+  T2.L = workspace_layout(n_rows, (int)n_tiles, T2.n_decode, hkv, G, c.head_dim);
+  T2.image.assign(T2.L.upload_end - T2.L.rows, 0);
+  memcpy(T2.image.data(), rows.data(), sizeof(RowInfo) * rows.size());
+  TileDesc* td = reinterpret_cast<TileDesc*>(T2.image.data() + (T2.L.tiles - T2.L.rows));
+  for (size_t i = 0; i < chunks.size(); ++i) td[i] = chunks[i].t;
+  for (size_t i = 0; i < decodes.size(); ++i) td[chunks.size() + i] = decodes[i];
+  // counters stay zero: every run starts its split tickets from 0
+  return MIXATTN_OK;
+}
+
+}  // namespace
+}  // namespace mixattn
+
+using namespace mixattn;
+
+struct mixattn_plan {
+  mixattn_kv_cache cache;
+  int32_t hq = 0, group = 0, log2_group = 0, n_rows = 0, max_pages = 0;
+  Tiling tiling;
+  uint8_t* host_buf = nullptr;  // pinned copy of tiling.image
+  size_t host_cap = 0;
+  cudaEvent_t copied = nullptr;
+  bool copy_recorded = false;
+};
+
+namespace {
+
+int plan_fill(mixattn_plan* p, int32_t n_rows, const int32_t* kinds, const int32_t* seq, const int32_t* off,
+              int32_t max_pages, size_t* ws_bytes) {
+  Tiling t;
+  int st = build_tiling(p->cache, p->hq, n_rows, kinds, seq, off, max_pages, &t);
+  if (st != MIXATTN_OK) return st;
+  // the previous run may still be copying from the pinned buffer
+  if (p->copy_recorded) {
+    if (cudaEventSynchronize(p->copied) != cudaSuccess) return MIXATTN_ERR_CUDA;
+    p->copy_recorded = false;
+  }
+  if (t.image.size() > p->host_cap) {
+    if (p->host_buf) cudaFreeHost(p->host_buf);
+    p->host_buf = nullptr;
+    p->host_cap = 0;
+    size_t cap = std::max<size_t>(t.image.size(), 4096);
+    if (cudaHostAlloc(reinterpret_cast<void**>(&p->host_buf), cap, cudaHostAllocDefault) != cudaSuccess) {
+      p->host_buf = nullptr;
+      return MIXATTN_ERR_CUDA;
+    }
+    p->host_cap = cap;
+  }
+  memcpy(p->host_buf, t.image.data(), t.image.size());
+  p->n_rows = n_rows;
+  p->max_pages = max_pages;
+  p->tiling = std::move(t);
+  if (ws_bytes) *ws_bytes = p->tiling.L.total;
+  return MIXATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mixattn_kv_cache_bytes(const mixattn_kv_cache* c, size_t plane_bytes_out[4]) {
+  if (check_cache_dims(c) != MIXATTN_OK) return 0;
+  const size_t rows = (size_t)c->num_pages * c->num_kv_heads * kPage;
+  const size_t kq = rows * quant_row_bytes(c->k_fmt, c->head_dim);
+  const size_t ks = rows * scale_row_bytes(c->k_fmt, c->head_dim);
+  const size_t vq = rows * quant_row_bytes(c->v_fmt, c->head_dim);
+  const size_t vs = rows * scale_row_bytes(c->v_fmt, c->head_dim);
+  if (plane_bytes_out) {
+    plane_bytes_out[0] = kq;
+    plane_bytes_out[1] = ks;
+    plane_bytes_out[2] = vq;
+    plane_bytes_out[3] = vs;
+  }
+  return kq + ks + vq + vs;
+}
+
+int mixattn_kv_append_quant(const mixattn_kv_cache* cache, const void* k_new, const void* v_new,
+                            const int32_t* slot_mapping, int32_t n_new, mixattn_stream stream) {
+  int st = check_cache(cache);
+  if (st != MIXATTN_OK) return st;
+  if (n_new < 0) return MIXATTN_ERR_INVALID_ARG;
+  if (n_new == 0) return MIXATTN_OK;
+  if (!k_new || !v_new || !slot_mapping) return MIXATTN_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 4)) return MIXATTN_ERR_INVALID_ARG;
+  unsigned int* err = error_word();
+  if (!err) return MIXATTN_ERR_CUDA;
+  cudaError_t e = launch_kv_append(*cache, k_new, v_new, slot_mapping, n_new, err,
+                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MIXATTN_OK : MIXATTN_ERR_CUDA;
+}
+
+int mixattn_kv_export_blocks(const mixattn_kv_cache* cache, int32_t which, const int32_t* slots, int32_t n,
+                             void* out, mixattn_stream stream) {
+  int st = check_cache(cache);
+  if (st != MIXATTN_OK) return st;
+  if ((which != 0 && which != 1) || n < 0) return MIXATTN_ERR_INVALID_ARG;
+  if (n == 0) return MIXATTN_OK;
+  if (!slots || !out || !aligned(slots, 4)) return MIXATTN_ERR_INVALID_ARG;
+  unsigned int* err = error_word();
+  if (!err) return MIXATTN_ERR_CUDA;
+  cudaError_t e = launch_kv_export(*cache, which, slots, n, out, err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MIXATTN_OK : MIXATTN_ERR_CUDA;
+}
+
+int mixattn_plan_create(mixattn_plan** plan_out, const mixattn_kv_cache* cache, int32_t num_q_heads,
+                        int32_t n_rows, const int32_t* row_kinds, const int32_t* seq_lens,
+                        const int32_t* q_offsets, int32_t max_pages, size_t* workspace_bytes) {
+  if (!plan_out) return MIXATTN_ERR_INVALID_ARG;
+  *plan_out = nullptr;
+  int st = check_cache(cache);
+  if (st != MIXATTN_OK) return st;
+  if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return MIXATTN_ERR_INVALID_ARG;
+  mixattn_plan* p = new mixattn_plan();
+  p->cache = *cache;
+  p->hq = num_q_heads;
+  p->group = num_q_heads / cache->num_kv_heads;
+  p->log2_group = 0;
+  while ((1 << p->log2_group) < p->group) ++p->log2_group;
+  st = plan_fill(p, n_rows, row_kinds, seq_lens, q_offsets, max_pages, workspace_bytes);
+  if (st == MIXATTN_OK && cudaEventCreateWithFlags(&p->copied, cudaEventDisableTiming) != cudaSuccess)
+    st = MIXATTN_ERR_CUDA;
+  if (st != MIXATTN_OK) {
+    mixattn_plan_destroy(p);
+    return st;
+  }
+  *plan_out = p;
+  return MIXATTN_OK;
+}
+
+int mixattn_plan_update(mixattn_plan* plan, int32_t n_rows, const int32_t* row_kinds, const int32_t* seq_lens,
+                        const int32_t* q_offsets, int32_t max_pages, size_t* workspace_bytes) {
+  if (!plan) return MIXATTN_ERR_INVALID_ARG;
+  return plan_fill(plan, n_rows, row_kinds, seq_lens, q_offsets, max_pages, workspace_bytes);
+}
+
+int mixattn_plan_info(const mixattn_plan* plan, int32_t* total_q, int32_t* n_chunk_tiles,
+                      int32_t* n_decode_tiles) {
+  if (!plan) return MIXATTN_ERR_INVALID_ARG;
+  if (total_q) *total_q = plan->tiling.total_q;
+  if (n_chunk_tiles) *n_chunk_tiles = plan->tiling.n_chunk;
+  if (n_decode_tiles) *n_decode_tiles = plan->tiling.n_decode;
+  return MIXATTN_OK;
+}
+
+int mixattn_run(const mixattn_plan* plan_c, const void* q, const int32_t* page_table, void* o, void* workspace,
+                size_t workspace_bytes, mixattn_stream stream) {
+  mixattn_plan* plan = const_cast<mixattn_plan*>(plan_c);
+  if (!plan) return MIXATTN_ERR_INVALID_ARG;
+  if (!q || !o || !page_table) return MIXATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(page_table, 4)) return MIXATTN_ERR_INVALID_ARG;
+  const WorkspaceLayout& L = plan->tiling.L;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return MIXATTN_ERR_WORKSPACE;
+  unsigned int* err = error_word();
+  if (!err) return MIXATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (cudaMemcpyAsync(ws + L.rows, plan->host_buf, L.upload_end - L.rows, cudaMemcpyHostToDevice, s) !=
+      cudaSuccess)
+    return MIXATTN_ERR_CUDA;
+  if (cudaEventRecord(plan->copied, s) != cudaSuccess) return MIXATTN_ERR_CUDA;
+  plan->copy_recorded = true;
+
+  AttnParams p;
+  const mixattn_kv_cache& c = plan->cache;
+  p.q = q;
+  p.o = o;
+  p.k_quant = static_cast<const uint8_t*>(c.k_quant);
+  p.k_scale = static_cast<const uint16_t*>(c.k_scale);
+  p.v_quant = static_cast<const uint8_t*>(c.v_quant);
+  p.v_scale = static_cast<const uint16_t*>(c.v_scale);
+  p.page_table = page_table;
+  p.rows = reinterpret_cast<const RowInfo*>(ws + L.rows);
+  p.tiles = reinterpret_cast<const TileDesc*>(ws + L.tiles);
+  p.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
+  p.partials = reinterpret_cast<float*>(ws + L.partials);
+  p.max_pages = plan->max_pages;
+  p.num_pages = c.num_pages;
+  p.n_chunk_tiles = plan->tiling.n_chunk;
+  p.n_decode_tiles = plan->tiling.n_decode;
+  p.hq = plan->hq;
+  p.hkv = c.num_kv_heads;
+  p.group = plan->group;
+  p.log2_group = plan->log2_group;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
+  cudaError_t e = dispatch_attention(c.k_fmt, c.v_fmt, c.head_dim, p, err, s);
+  return e == cudaSuccess ? MIXATTN_OK : MIXATTN_ERR_CUDA;
+}
+
+void mixattn_plan_destroy(mixattn_plan* plan) {
+  if (!plan) return;
+  if (plan->copy_recorded && plan->copied) cudaEventSynchronize(plan->copied);
+  if (plan->copied) cudaEventDestroy(plan->copied);
+  if (plan->host_buf) cudaFreeHost(plan->host_buf);
+  delete plan;
+}
+
+int mixattn_workspace_bytes(const mixattn_kv_cache* cache, int32_t num_q_heads, int32_t n_rows,
+                            const int32_t* row_kinds, const int32_t* seq_lens, const int32_t* q_offsets,
+                            int32_t max_pages, size_t* workspace_bytes) {
+  int st = check_cache_dims(cache);
+  if (st != MIXATTN_OK) return st;
+  if (!workspace_bytes) return MIXATTN_ERR_INVALID_ARG;
+  Tiling t;
+  st = build_tiling(*cache, num_q_heads, n_rows, row_kinds, seq_lens, q_offsets, max_pages, &t);
+  if (st != MIXATTN_OK) return st;
+  *workspace_bytes = t.L.total;
+  return MIXATTN_OK;
+}
+
+int mixattn_mixed_attention(const mixattn_kv_cache* cache, int32_t num_q_heads, const void* q,
+                            const int32_t* page_table, int32_t max_pages, int32_t n_rows, const int32_t* seq_lens,
+                            const int32_t* q_offsets, const int32_t* row_kinds, void* o, void* workspace,
+                            size_t workspace_bytes, mixattn_stream stream) {
+  mixattn_plan* plan = nullptr;
+  int st = mixattn_plan_create(&plan, cache, num_q_heads, n_rows, row_kinds, seq_lens, q_offsets, max_pages,
+                               nullptr);
+  if (st != MIXATTN_OK) return st;
+  st = mixattn_run(plan, q, page_table, o, workspace, workspace_bytes, stream);
+  mixattn_plan_destroy(plan);  // waits for the tile-list copy only
+  return st;
+}
+
+int64_t mixattn_device_error(int32_t clear) {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return MIXATTN_ERR_CUDA;
+  if (clear) {
+    const unsigned int z = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &z, sizeof(z)) != cudaSuccess) return MIXATTN_ERR_CUDA;
+  }
+  return (int64_t)v;
+}
+
+const char* mixattn_status_string(int32_t status) {
+  switch (status) {
+    case MIXATTN_OK: return "ok";
+    case MIXATTN_ERR_INVALID_ARG: return "invalid argument";
+    case MIXATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MIXATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MIXATTN_ERR_CUDA: return "CUDA runtime error";
+    case MIXATTN_ERR_DEVICE_CHECK: return "device-side check failed";
+    default: return "unknown status";
+  }
+}
+
+int32_t mixattn_version(void) { return 100; }
+
+}  // extern "C"

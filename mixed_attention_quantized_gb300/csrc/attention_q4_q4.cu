@@ -1,0 +1,13 @@
+// attention_q4_q4.cu -- instantiation of the mixed-batch attention kernels for
+// K format MIXATTN_KV_Q4_0 and V format MIXATTN_KV_Q4_0 (one translation unit per format pair so the
+// build compiles them in parallel).
+#include "attention_kernel.cuh"
+
+namespace mixattn {
+
+cudaError_t launch_attention_q4_q4(int head_dim, const AttnParams& p, unsigned int* err, cudaStream_t s) {
+  if (head_dim == 64) return launch_attention_t<MIXATTN_KV_Q4_0, MIXATTN_KV_Q4_0, 64>(p, err, s);
+  return launch_attention_t<MIXATTN_KV_Q4_0, MIXATTN_KV_Q4_0, 128>(p, err, s);
+}
+
+}  // namespace mixattn

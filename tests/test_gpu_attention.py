@@ -1,0 +1,158 @@
+"""Parity of the mixed-batch attention step (CUDA, through the C ABI) with the
+fp64 oracle over the oracle-dequantised cache, plus the invariants the
+reference page relies on (page "自研RDNA高併發推論引擎 以AI Max+ 395為範例":
+§1 mixed batch and bit-identical greedy output under concurrency; §2 blocked
+KV formats).  Bar: max |o_gpu - o_oracle| <= 2e-3 on fp16 outputs."""
+import numpy as np
+import pytest
+
+import workloads as wl
+from _harness import TOL, build_cache, max_err, oracle_attention, run_attention
+
+pytestmark = pytest.mark.gpu
+
+PAIRS = [(wl.FMT_Q8_0, wl.FMT_Q8_0), (wl.FMT_Q4_0, wl.FMT_Q4_0), (wl.FMT_F16, wl.FMT_F16),
+         (wl.FMT_Q8_0, wl.FMT_Q4_0), (wl.FMT_Q4_0, wl.FMT_Q8_0)]
+D, C = wl.ROW_DECODE, wl.ROW_CHUNK
+
+
+@pytest.mark.parametrize("kf,vf", PAIRS)
+def test_tiny_config_matches_oracle(kf, vf):
+    w = wl.tiny(kf, vf)
+    cache, pt = build_cache(w)
+    got = run_attention(w, cache, pt)
+    ref = oracle_attention(w)
+    assert max_err(got, ref) <= TOL
+
+
+def _ragged(kf, vf, hq, hkv, d, seed):
+    rows = [(D, 1, 0), (D, 31, 30), (D, 32, 31), (D, 33, 32), (C, 100, 37), (D, 1000, 999),
+            (C, 45, 0), (C, 300, 500 - 200), (D, 4097, 4096), (C, 1, 0), (C, 129, 127)]
+    return wl.custom(f"ragged_g{hq // hkv}_d{d}", hq, hkv, d, kf, vf, seed, rows, n_outlier=2,
+                     spare_pages=7)
+
+
+@pytest.mark.parametrize("kf,vf", PAIRS)
+@pytest.mark.parametrize("hq,hkv,d", [(16, 4, 128), (8, 8, 64), (16, 8, 128), (16, 2, 64)])
+def test_ragged_batches_match_oracle(kf, vf, hq, hkv, d):
+    w = _ragged(kf, vf, hq, hkv, d, seed=hq * 100 + hkv * 10 + d + kf * 3 + vf)
+    cache, pt = build_cache(w, fill=0xFF)  # stale slots hold NaN patterns
+    got = run_attention(w, cache, pt)
+    ref = oracle_attention(w)
+    assert max_err(got, ref) <= TOL
+
+
+def test_stale_slots_do_not_change_a_bit():
+    for kf, vf in PAIRS:
+        w = _ragged(kf, vf, 16, 4, 128, seed=77)
+        c0, pt = build_cache(w, fill=0)
+        c1, _ = build_cache(w, fill=0xFF)
+        assert np.array_equal(run_attention(w, c0, pt), run_attention(w, c1, pt))
+
+
+def test_page_placement_does_not_change_a_bit():
+    w = _ragged(wl.FMT_Q8_0, wl.FMT_Q8_0, 16, 4, 128, seed=5)
+    c0, pt0 = build_cache(w)
+    perm = np.random.default_rng(99).permutation(w.num_pages).astype(np.int32)
+    pt1 = np.where(pt0 >= 0, perm[np.maximum(pt0, 0)], -1).astype(np.int32)
+    c1, _ = build_cache(w, pt=pt1)
+    assert np.array_equal(run_attention(w, c0, pt0), run_attention(w, c1, pt1))
+
+
+def test_a_row_gives_the_same_bits_alone_and_in_a_batch():
+    """The page's greedy outputs stay bit-identical when a request runs alone or
+    concurrently; here: a row's output does not depend on the rest of the batch."""
+    kf = vf = wl.FMT_Q4_0
+    rows = [(D, 5000, 4999), (C, 700, 300), (D, 77, 76), (C, 64, 0), (D, 40000, 39999)]
+    w = wl.custom("batch", 32, 8, 128, kf, vf, 11, rows)
+    import torch
+    cache, pt = build_cache(w)
+    full = run_attention(w, cache, pt)
+    q = wl.queries(w)
+    starts = w.q_starts
+    for r in (0, 1, 4):
+        sub = wl.custom("one", 32, 8, 128, kf, vf, 11, [rows[r]])
+        qr = torch.from_numpy(q[starts[r]:starts[r] + w.q_lens[r]].copy()).cuda()
+        alone = run_attention(sub, cache, pt[r:r + 1], q=qr)
+        assert np.array_equal(alone, full[starts[r]:starts[r] + w.q_lens[r]])
+
+
+def test_decode_row_matches_last_row_of_the_same_chunk():
+    kf = vf = wl.FMT_Q8_0
+    wc = wl.custom("c", 32, 8, 128, kf, vf, 21, [(C, 3000, 2000)])
+    wd = wl.custom("c", 32, 8, 128, kf, vf, 21, [(D, 3000, 2999)])
+    cache, pt = build_cache(wc)
+    oc = run_attention(wc, cache, pt)
+    from workloads import row_q
+    import torch
+    qd = torch.from_numpy(row_q(wc, 0)[-1:].copy()).cuda()
+    od = run_attention(wd, cache, pt, q=qd)
+    assert np.abs(oc[-1].astype(np.float64) - od[0].astype(np.float64)).max() <= TOL
+    ref = oracle_attention(wc, sel=[999])
+    assert max_err(od, ref) <= TOL and max_err(oc[-1:], ref) <= TOL
+
+
+def test_bad_page_id_sets_the_device_error():
+    import torch
+    import mixed_attention_quantized_gb300 as mq
+    w = wl.custom("bad", 8, 2, 64, wl.FMT_Q8_0, wl.FMT_Q8_0, 3, [(D, 100, 99), (C, 80, 40)])
+    cache, pt = build_cache(w)
+    mq.device_error(clear=True)
+    bad = pt.copy()
+    bad[0, 1] = w.num_pages + 5
+    bad[1, 0] = -3
+    out = run_attention(w, cache, bad)
+    assert mq.device_error(clear=True) & mq.DEVERR_PAGE_ID
+    # the error is reported; the good pages still produced numbers of the right shape
+    assert out.shape == (w.total_q, 8, 64)
+    assert mq.device_error(clear=True) == 0
+
+
+def test_one_call_entry_point_matches_the_plan_path():
+    import torch
+    import mixed_attention_quantized_gb300 as mq
+    w = _ragged(wl.FMT_Q8_0, wl.FMT_Q4_0, 16, 4, 128, seed=1)
+    cache, pt = build_cache(w)
+    q = torch.from_numpy(wl.queries(w)).cuda()
+    o = mq.mixed_attention(cache, q, torch.from_numpy(pt).cuda(), w.seq_lens, w.q_offsets, w.row_kinds)
+    torch.cuda.synchronize()
+    assert np.array_equal(o.cpu().numpy(), run_attention(w, cache, pt))
+
+
+def test_plan_update_and_reuse_across_layers():
+    import torch
+    import mixed_attention_quantized_gb300 as mq
+    w1 = _ragged(wl.FMT_Q8_0, wl.FMT_Q8_0, 16, 4, 128, seed=2)
+    cache, pt = build_cache(w1)
+    ref1 = run_attention(w1, cache, pt)
+    plan = mq.Plan(cache, 16, w1.row_kinds, w1.seq_lens, w1.q_offsets, pt.shape[1])
+    ws = mq.alloc_workspace(plan.workspace_bytes)
+    q = torch.from_numpy(wl.queries(w1)).cuda()
+    ptd = torch.from_numpy(pt).cuda()
+    outs = []
+    for _ in range(3):  # same plan, three "layers"
+        o = torch.empty_like(q)
+        plan.run(q, ptd, o, ws)
+        outs.append(o)
+    torch.cuda.synchronize()
+    for o in outs:
+        assert np.array_equal(o.cpu().numpy(), ref1)
+    # re-tile for a smaller batch (first two rows)
+    plan.update(w1.row_kinds[:2], w1.seq_lens[:2], w1.q_offsets[:2], pt.shape[1])
+    o2 = torch.empty_like(q[:2])
+    plan.run(q[:2], ptd[:2], o2, mq.alloc_workspace(plan.workspace_bytes))
+    torch.cuda.synchronize()
+    assert np.array_equal(o2.cpu().numpy(), ref1[:2])
+    plan.close()
+
+
+def test_workspace_too_small_is_rejected():
+    import torch
+    import mixed_attention_quantized_gb300 as mq
+    w = wl.tiny()
+    cache, pt = build_cache(w)
+    plan = mq.Plan(cache, 4, w.row_kinds, w.seq_lens, w.q_offsets, pt.shape[1])
+    q = torch.from_numpy(wl.queries(w)).cuda()
+    with pytest.raises(mq.MixattnError) as e:
+        plan.run(q, torch.from_numpy(pt).cuda(), torch.empty_like(q), mq.alloc_workspace(plan.workspace_bytes - 256))
+    assert e.value.status == mq.ERR_WORKSPACE
