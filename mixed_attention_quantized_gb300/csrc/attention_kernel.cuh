@@ -19,10 +19,12 @@
 //
 // Chunk tiles (tensor-bound): a CTA owns 128 rows = 128/G query tokens x G
 // heads of one kv head.  K/V pages arrive raw through 1-D bulk copies (TMA
-// engine) into a double-buffered stage, are dequantised to fp16 into
-// 128-byte-swizzled tiles, S = Q K^T and O += P V run on tcgen05.mma with the
-// accumulators in TMEM, and the softmax threads own one TMEM lane (one query
-// row) each.
+// engine) into a stage whose refill overlaps the math of the previous tile.
+// They are dequantised into 128-byte-swizzled fp16 tiles -- an exact hi/lo
+// pair for quantised formats, since d*q needs up to 18 significant bits --
+// and S = Q K^T and O += P V run on tcgen05.mma (one MMA per half) with the
+// accumulators in TMEM.  The softmax threads own one TMEM lane (one query row)
+// each and write P as fp16 back into TMEM, where the PV MMA reads it.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -45,21 +47,25 @@ struct ChunkSmem {
   static constexpr int kVqPage = kPage * (FV == MIXATTN_KV_F16 ? 2 * D : (FV == MIXATTN_KV_Q8_0 ? D : D / 2));
   static constexpr int kVsPage = FV == MIXATTN_KV_F16 ? 0 : kPage * kNb * 2;
   static constexpr int kPagesPerTile = kChunkN / kPage;  // 4
+  // quantised formats carry an exact low half: d*q = hi + lo, both fp16
+  static constexpr bool kKLo = FK != MIXATTN_KV_F16;
+  static constexpr bool kVLo = FV != MIXATTN_KV_F16;
   // raw stage: [Kq x4][Ks x4][Vq x4][Vs x4]
   static constexpr int kRawKq = 0;
   static constexpr int kRawKs = kRawKq + kPagesPerTile * kKqPage;
   static constexpr int kRawVq = kRawKs + kPagesPerTile * kKsPage;
   static constexpr int kRawVs = kRawVq + kPagesPerTile * kVqPage;
   static constexpr int kRawBytes = (kRawVs + kPagesPerTile * kVsPage + 1023) / 1024 * 1024;
+  static constexpr int kTile = kChunkN * D * 2;             // one fp16 operand tile
   static constexpr int kQ = 0;                              // [D/64][128 rows][128 B]
-  static constexpr int kK = kQ + kChunkM * D * 2;           // [D/64][128 keys][128 B]
-  static constexpr int kV = kK + kChunkN * D * 2;           // [D/64][128 keys][128 B]
-  static constexpr int kP = kV + kChunkN * D * 2;           // [2][128 rows][128 B]
-  static constexpr int kRaw = kP + kChunkM * kChunkN * 2;
-  static constexpr int kFixed = kRaw + 1024;                // + barriers
-  static constexpr int kStages = (kFixed + 2 * kRawBytes <= 227 * 1024) ? 2 : 1;
-  static constexpr int kBar = kRaw + kStages * kRawBytes;
+  static constexpr int kKh = kQ + kChunkM * D * 2;          // [D/64][128 keys][128 B]
+  static constexpr int kKl = kKh + kTile;
+  static constexpr int kVh = kKl + (kKLo ? kTile : 0);
+  static constexpr int kVl = kVh + kTile;
+  static constexpr int kRaw = kVl + (kVLo ? kTile : 0);
+  static constexpr int kBar = kRaw + kRawBytes;
   static constexpr int kTotal = kBar + 64 + 1024;           // + slack for 1024-B alignment
+  static_assert(kTotal <= 227 * 1024, "chunk tile does not fit in shared memory");
 };
 
 // Merge scratch of a decode tile: per warp m[8], l[8], O[8][D].
@@ -466,11 +472,21 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int cc) {
   return (uint32_t)(row * 128 + ((cc ^ (row & 7)) << 4));
 }
 
-// Dequantise one 128-key x D tile from a raw stage into a swizzled fp16 tile.
-// Keys at or past `valid_keys` (relative to the tile) are written as zeros.
-template <int F, int D>
-__device__ __forceinline__ void dequant_tile(const uint8_t* raw_q, const uint8_t* raw_s, uint8_t* dst,
-                                             int valid_keys) {
+// v holds exact small integers (f16x2), s the fp16 scale in both halves.
+// hi = fp16(v*s); lo = v*s - hi, which is exact in fp16: v*s has at most
+// 18 significant bits, hi keeps the top 11, and the residual is a multiple of
+// the scale's ulp (>= 2^-24) below 2^8 of them.  So hi + lo == v*s exactly.
+__device__ __forceinline__ void split_hilo(uint32_t v, uint32_t s, uint32_t& hi, uint32_t& lo) {
+  hi = hmul2_u32(v, s);
+  lo = hfma2_u32(v, s, hi ^ 0x80008000u);
+}
+
+// Dequantise one 128-key x D tile from the raw stage into swizzled fp16 tiles
+// (hi, and lo for quantised formats).  Keys at or past `valid_keys` (relative
+// to the tile) are written as zeros.
+template <int F, int D, bool LO>
+__device__ __forceinline__ void dequant_tile(const uint8_t* raw_q, const uint8_t* raw_s, uint8_t* dst_hi,
+                                             uint8_t* dst_lo, int valid_keys) {
   constexpr int NB = D / kBlock;
   constexpr int CPR = D / 8;  // 16-byte fp16 chunks per key row
   constexpr int RB = F == MIXATTN_KV_F16 ? 2 * D : (F == MIXATTN_KV_Q8_0 ? D : D / 2);
@@ -479,11 +495,11 @@ __device__ __forceinline__ void dequant_tile(const uint8_t* raw_q, const uint8_t
   for (int k = threadIdx.x; k < kChunkN * CPR; k += kThreads) {
     const int key = k / CPR, dc = k - key * CPR;
     const int pj = key >> 5, kr = key & 31;
-    uint4 outv = make_uint4(0u, 0u, 0u, 0u);
+    uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = make_uint4(0u, 0u, 0u, 0u);
     if (key < valid_keys) {
       const uint8_t* qrow = raw_q + pj * PAGE_Q + kr * RB;
       if (F == MIXATTN_KV_F16) {
-        outv = *reinterpret_cast<const uint4*>(qrow + 16 * dc);
+        hi = *reinterpret_cast<const uint4*>(qrow + 16 * dc);
       } else {
         const int b = dc >> 2;
         const uint16_t sh = *reinterpret_cast<const uint16_t*>(raw_s + pj * PAGE_S + (kr * NB + b) * 2);
@@ -500,14 +516,16 @@ __device__ __forceinline__ void dequant_tile(const uint8_t* raw_q, const uint8_t
           u4x4_to_f16x2x2((w.x >> shift) & 0x0F0F0F0Fu, h0, h1);
           u4x4_to_f16x2x2((w.y >> shift) & 0x0F0F0F0Fu, h2, h3);
         }
-        outv.x = hmul2_u32(h0, s2);
-        outv.y = hmul2_u32(h1, s2);
-        outv.z = hmul2_u32(h2, s2);
-        outv.w = hmul2_u32(h3, s2);
+        split_hilo(h0, s2, hi.x, lo.x);
+        split_hilo(h1, s2, hi.y, lo.y);
+        split_hilo(h2, s2, hi.z, lo.z);
+        split_hilo(h3, s2, hi.w, lo.w);
       }
     }
     const int half = dc >> 3, cc = dc & 7;
-    *reinterpret_cast<uint4*>(dst + half * (kChunkN * 128) + sw128_off(key, cc)) = outv;
+    const uint32_t off = half * (kChunkN * 128) + sw128_off(key, cc);
+    *reinterpret_cast<uint4*>(dst_hi + off) = hi;
+    if (LO) *reinterpret_cast<uint4*>(dst_lo + off) = lo;
   }
 }
 
@@ -516,14 +534,14 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
                                            unsigned int* err) {
   using L = ChunkSmem<FK, FV, D>;
   constexpr int NB = D / kBlock;
-  constexpr uint32_t kTmemCols = 256;  // S: 128 columns, O: D columns
+  constexpr uint32_t kTmemCols = 256;  // S: 128 columns (P, fp16, overwrites its first 64); O: D columns
   constexpr uint32_t kSCol = 0, kOCol = 128;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);  // [2]
-  uint64_t* s_done = full + 2;
-  uint64_t* o_done = full + 3;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 4);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* s_done = full + 1;
+  uint64_t* o_done = full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 3);
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int G = p.group, lg = p.log2_group;
@@ -536,8 +554,7 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
   const int32_t* pt_row = p.page_table + (int64_t)t.row * p.max_pages;
 
   if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+    mbar_init(full, 1);
     mbar_init(s_done, 1);
     mbar_init(o_done, 1);
     fence_mbar_init();
@@ -562,14 +579,15 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
       *reinterpret_cast<uint4*>(smem + L::kQ + (dc >> 3) * (kChunkM * 128) + sw128_off(row, dc & 7)) = v;
     }
   }
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // ---- producer: raw pages of KV tile jj into stage st ----
-  auto issue_raw = [&](int jj, int st) {
-    uint8_t* raw = smem + L::kRaw + st * L::kRawBytes;
+  // ---- producer: raw pages of KV tile jj into the stage ----
+  auto issue_raw = [&](int jj) {
+    uint8_t* raw = smem + L::kRaw;
     uint32_t bytes = 0;
     int pids[L::kPagesPerTile];
 #pragma unroll
@@ -586,27 +604,27 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
       pids[pj] = pid;
       if (pid >= 0) bytes += L::kKqPage + L::kKsPage + L::kVqPage + L::kVsPage;
     }
-    mbar_arrive_expect_tx(&full[st], bytes);
+    mbar_arrive_expect_tx(full, bytes);
 #pragma unroll
     for (int pj = 0; pj < L::kPagesPerTile; ++pj) {
       const int pid = pids[pj];
       if (pid < 0) continue;
       const int64_t prow = ((int64_t)pid * p.hkv + g) * kPage;  // first plane row of (page, head)
-      bulk_g2s(raw + L::kRawKq + pj * L::kKqPage, p.k_quant + prow * (L::kKqPage / kPage), L::kKqPage, &full[st]);
-      if (L::kKsPage)
-        bulk_g2s(raw + L::kRawKs + pj * L::kKsPage, p.k_scale + prow * NB, L::kKsPage, &full[st]);
-      bulk_g2s(raw + L::kRawVq + pj * L::kVqPage, p.v_quant + prow * (L::kVqPage / kPage), L::kVqPage, &full[st]);
-      if (L::kVsPage)
-        bulk_g2s(raw + L::kRawVs + pj * L::kVsPage, p.v_scale + prow * NB, L::kVsPage, &full[st]);
+      bulk_g2s(raw + L::kRawKq + pj * L::kKqPage, p.k_quant + prow * (L::kKqPage / kPage), L::kKqPage, full);
+      if (L::kKsPage) bulk_g2s(raw + L::kRawKs + pj * L::kKsPage, p.k_scale + prow * NB, L::kKsPage, full);
+      bulk_g2s(raw + L::kRawVq + pj * L::kVqPage, p.v_quant + prow * (L::kVqPage / kPage), L::kVqPage, full);
+      if (L::kVsPage) bulk_g2s(raw + L::kRawVs + pj * L::kVsPage, p.v_scale + prow * NB, L::kVsPage, full);
     }
   };
 
   const int issuer = 128;  // warp 4, lane 0: copies and MMAs
+  int raw_issued = 0, raw_consumed = 0;
   if (tid == issuer) {
-    for (int jj = 0; jj < L::kStages && jj < n_kv; ++jj) issue_raw(jj, jj);
+    issue_raw(0);
+    raw_issued = 1;
   }
 
-  // softmax state: thread i < 128 owns row i
+  // softmax state: thread i < 128 owns row i (TMEM lane i)
   const int row = tid & 127;
   const int tok = row >> lg;
   const bool row_valid = tid < 128 && tok < t.count;
@@ -619,33 +637,38 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
 
   constexpr uint32_t kIdescQK = idesc_f16_f32(128, kChunkN, false, false);
   constexpr uint32_t kIdescPV = idesc_f16_f32(128, D, false, true);
-  const uint32_t sQ = smem_u32(smem + L::kQ), sK = smem_u32(smem + L::kK);
-  const uint32_t sV = smem_u32(smem + L::kV), sP = smem_u32(smem + L::kP);
+  const uint32_t sQ = smem_u32(smem + L::kQ);
+  const uint32_t sKh = smem_u32(smem + L::kKh), sKl = smem_u32(smem + L::kKl);
+  const uint32_t sVh = smem_u32(smem + L::kVh), sVl = smem_u32(smem + L::kVl);
 
-  for (int j = 0; j < n_kv && ok; ++j) {
-    const int st = j % L::kStages;
-    ok = mbar_wait(&full[st], (uint32_t)((j / L::kStages) & 1), err);
-    if (j > 0) ok = ok && mbar_wait(o_done, (uint32_t)((j - 1) & 1), err);
+  for (int j = 0; j < n_kv; ++j) {
+    ok = mbar_wait(full, (uint32_t)(j & 1), err) && ok;
+    raw_consumed = j + 1;
+    if (j > 0) ok = mbar_wait(o_done, (uint32_t)((j - 1) & 1), err) && ok;
     tc_fence_after();
-    const uint8_t* raw = smem + L::kRaw + st * L::kRawBytes;
+    const uint8_t* raw = smem + L::kRaw;
     const int valid_keys = key_end - j * kChunkN;
-    dequant_tile<FK, D>(raw + L::kRawKq, raw + L::kRawKs, smem + L::kK, valid_keys);
-    dequant_tile<FV, D>(raw + L::kRawVq, raw + L::kRawVs, smem + L::kV, valid_keys);
+    dequant_tile<FK, D, L::kKLo>(raw + L::kRawKq, raw + L::kRawKs, smem + L::kKh, smem + L::kKl, valid_keys);
+    dequant_tile<FV, D, L::kVLo>(raw + L::kRawVq, raw + L::kRawVs, smem + L::kVh, smem + L::kVl, valid_keys);
     fence_proxy_async_smem();
     __syncthreads();
     if (tid == issuer) {
-      if (j + L::kStages < n_kv) issue_raw(j + L::kStages, st);
+      if (j + 1 < n_kv) {  // the stage is free again: the copy overlaps this tile's math
+        issue_raw(j + 1);
+        raw_issued = j + 2;
+      }
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         const uint32_t off = (uint32_t)((ks >> 2) * (128 * 128) + (ks & 3) * 32);
-        tc_mma_ss(tmem + kSCol, sw128_desc(sQ + off, 16, 1024), sw128_desc(sK + off, 16, 1024), kIdescQK,
-                  ks > 0 ? 1u : 0u);
+        const uint64_t qd = sw128_desc(sQ + off, 16, 1024);
+        tc_mma_ss(tmem + kSCol, qd, sw128_desc(sKh + off, 16, 1024), kIdescQK, ks > 0 ? 1u : 0u);
+        if (L::kKLo) tc_mma_ss(tmem + kSCol, qd, sw128_desc(sKl + off, 16, 1024), kIdescQK, 1u);
       }
       tc_commit(s_done);
     }
     if (tid < 128) {
-      ok = ok && mbar_wait(s_done, (uint32_t)(j & 1), err);
+      ok = mbar_wait(s_done, (uint32_t)(j & 1), err) && ok;
       tc_fence_after();
       const int kbase = j * kChunkN;
       // pass 1: row max of the scaled, masked scores
@@ -664,7 +687,7 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
       }
       const float m_new = fmaxf(m_run, mx);
       const float alpha = ex2(m_run - m_new);
-      // pass 2: P = 2^(s - m) as fp16 into the swizzled P tile, row sums
+      // pass 2: P = 2^(s - m) as fp16 into TMEM over the consumed scores, row sums
       float sum = 0.f;
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
@@ -681,12 +704,7 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
           sum += p0 + p1;
           pk[e >> 1] = pack_f16x2(p0, p1);
         }
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int kc = ch * 4 + q4;  // 8-key chunk index 0..15
-          *reinterpret_cast<uint4*>(smem + L::kP + (kc >> 3) * (kChunkM * 128) + sw128_off(row, kc & 7)) =
-              make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-        }
+        tmem_st16(tmem + lane_base + kSCol + 16 * ch, pk);
       }
       l_run = l_run * alpha + sum;
       m_run = m_new;
@@ -701,9 +719,8 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
           for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
           tmem_st32(tmem + lane_base + kOCol + 32 * ch, v);
         }
-        tmem_wait_st();
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
     }
     tc_fence_before();
     if (!__syncthreads_and(ok)) {  // a bounded wait gave up somewhere: leave together
@@ -714,10 +731,11 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < kChunkN / 16; ++kk) {
-        const uint32_t aoff = (uint32_t)((kk >> 2) * (kChunkM * 128) + (kk & 3) * 32);
+        const uint32_t pa = tmem + kSCol + 8 * kk;  // P columns of keys 16kk..16kk+15
         const uint32_t boff = (uint32_t)(kk * 16 * 128);
-        tc_mma_ss(tmem + kOCol, sw128_desc(sP + aoff, 16, 1024), sw128_desc(sV + boff, kChunkN * 128, 1024),
-                  kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+        tc_mma_ts(tmem + kOCol, pa, sw128_desc(sVh + boff, kChunkN * 128, 1024), kIdescPV, acc);
+        if (L::kVLo) tc_mma_ts(tmem + kOCol, pa, sw128_desc(sVl + boff, kChunkN * 128, 1024), kIdescPV, 1u);
       }
       tc_commit(o_done);
       ++pv_issued;
@@ -725,13 +743,12 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
   }
 
   // ---- epilogue: O / l -> fp16 ----
-  if (tid < 128 || tid == issuer) {
-    // the issuer also waits, so no MMA is still writing TMEM when it is freed
-    if (pv_issued > 0 || tid < 128) {
-      const int last = ok ? n_kv - 1 : -1;
-      if (last >= 0) ok = mbar_wait(o_done, (uint32_t)(last & 1), err);
-    }
+  if (tid == issuer) {
+    // nothing the issuer started may still be running when TMEM and the stage are released
+    if (pv_issued > 0) mbar_wait(o_done, (uint32_t)((pv_issued - 1) & 1), err);
+    if (raw_issued > raw_consumed) mbar_wait(full, (uint32_t)((raw_issued - 1) & 1), err);
   }
+  if (tid < 128 && ok) ok = mbar_wait(o_done, (uint32_t)((n_kv - 1) & 1), err);
   if (tid < 128) {
     tc_fence_after();
     const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;

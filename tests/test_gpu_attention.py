@@ -27,7 +27,7 @@ def test_tiny_config_matches_oracle(kf, vf):
 
 def _ragged(kf, vf, hq, hkv, d, seed):
     rows = [(D, 1, 0), (D, 31, 30), (D, 32, 31), (D, 33, 32), (C, 100, 37), (D, 1000, 999),
-            (C, 45, 0), (C, 300, 500 - 200), (D, 4097, 4096), (C, 1, 0), (C, 129, 127)]
+            (C, 45, 0), (C, 500, 200), (D, 4097, 4096), (C, 1, 0), (C, 129, 127)]
     return wl.custom(f"ragged_g{hq // hkv}_d{d}", hq, hkv, d, kf, vf, seed, rows, n_outlier=2,
                      spare_pages=7)
 
