@@ -8,9 +8,10 @@
 // over the dequantised cache values k^, v^ (§2 blocked formats).
 //
 // Decode tiles (HBM-bound, ~7.5 FLOP per byte): a CTA of 8 warps walks a page
-// range of one (row, kv head); each warp streams its pages with 16-byte-class
-// vector loads straight into registers and runs QK^T and PV on mma.sync
-// m16n8k16 with the G query heads in the N=8 dimension.  Quantised codes are
+// range of one (row, kv head).  Each warp keeps several 16-key M-tiles in
+// flight through a cp.async ring in shared memory (16-byte chunks, 128-byte
+// XOR swizzle so the fragment reads are conflict free) and runs QK^T and PV on
+// mma.sync m16n8k16 with the G query heads in the N=8 dimension.  Quantised codes are
 // turned into exact fp16 integers by a byte permute (no rounding); the Q8_0 /
 // Q4_0 scales are applied in fp32: per key and 32-d block on the scores, and
 // folded into P per key and block on the values.  Warp partials are merged in
@@ -68,18 +69,40 @@ struct ChunkSmem {
   static_assert(kTotal <= 227 * 1024, "chunk tile does not fit in shared memory");
 };
 
-// Merge scratch of a decode tile: per warp m[8], l[8], O[8][D].
-template <int D>
+// Staging ring of a decode warp: one stage = one M-tile (16 keys) of one page:
+// the 16 contiguous K and V rows of the page plane, copied cooperatively in
+// 16-byte chunks and placed with a 128-byte XOR swizzle (16-byte chunk index ^=
+// 128-byte line index mod 8), so the fragment reads of every format are
+// bank-conflict free; then the 16 keys' K and V scale rows.
+template <int FK, int FV, int D>
 struct DecodeSmem {
+  static constexpr int kNb = D / kBlock;
+  static constexpr int kRbK = FK == MIXATTN_KV_F16 ? 2 * D : (FK == MIXATTN_KV_Q8_0 ? D : D / 2);
+  static constexpr int kRbV = FV == MIXATTN_KV_F16 ? 2 * D : (FV == MIXATTN_KV_Q8_0 ? D : D / 2);
+  static constexpr int kSc = 16 * kNb * 2;  // 16 keys x D/32 fp16 scales
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + 16 * kRbK;
+  static constexpr int kKs = kV + 16 * kRbV;
+  static constexpr int kVs = kKs + (FK == MIXATTN_KV_F16 ? 0 : kSc);
+  static constexpr int kStage = (kVs + (FV == MIXATTN_KV_F16 ? 0 : kSc) + 127) / 128 * 128;
+  static constexpr int kBudget = 212 * 1024;
+  static constexpr int kStagesRaw = kBudget / (kWarps * kStage);
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : (kStagesRaw < 2 ? 2 : kStagesRaw);
+  static constexpr int kRing = kWarps * kStages * kStage;
+  // after the page loop the same memory holds the warp partials: m[8], l[8], O[8][D]
   static constexpr int kPerWarp = 16 + kMaxGroup * D;
-  static constexpr int kTotal = kWarps * kPerWarp * 4 + 16;
+  static constexpr int kMerge = kWarps * kPerWarp * 4;
+  static constexpr int kTotal = (kRing > kMerge ? kRing : kMerge) + 16;
+  static_assert(kTotal <= 227 * 1024, "decode staging does not fit in shared memory");
 };
+
+// 128-byte XOR swizzle of a byte offset inside a staged region.
+__device__ __forceinline__ int swz(int o) { return o ^ (((o >> 7) & 7) << 4); }
 
 // ===========================================================================
 // Decode tiles
 // ===========================================================================
 
-// Byte offset of token `key` (0..31) of a page-plane row, for K/V row bytes.
 template <int F, int D>
 __device__ __forceinline__ constexpr int row_bytes() {
   return F == MIXATTN_KV_F16 ? 2 * D : (F == MIXATTN_KV_Q8_0 ? D : D / 2);
@@ -94,11 +117,34 @@ __device__ __forceinline__ int pv_row_to_d(int t, int rr) {
   return 32 * b + 4 * r + 2 * u + hi;
 }
 
+__device__ __forceinline__ void unpack_scales(uint2 a, float* out) {
+  out[0] = __half2float(__ushort_as_half(a.x & 0xFFFF));
+  out[1] = __half2float(__ushort_as_half(a.x >> 16));
+  out[2] = __half2float(__ushort_as_half(a.y & 0xFFFF));
+  out[3] = __half2float(__ushort_as_half(a.y >> 16));
+}
+
+template <int NB>
+__device__ __forceinline__ void load_scales(const uint8_t* p, float (&out)[NB]) {
+  if (NB == 4) {
+    float t[4];
+    unpack_scales(lds64(p), t);
+#pragma unroll
+    for (int i = 0; i < NB; ++i) out[i] = t[i];
+  } else {
+    const uint32_t a = lds32(p);
+    out[0] = __half2float(__ushort_as_half(a & 0xFFFF));
+    out[NB - 1] = __half2float(__ushort_as_half(a >> 16));
+  }
+}
+
 template <int FK, int FV, int D>
 __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc& t, int dec_idx, uint8_t* smem,
                                             unsigned int* err) {
+  using S = DecodeSmem<FK, FV, D>;
   constexpr int NB = D / kBlock;   // scale blocks per row
   constexpr int KS = D / 16;       // k-steps of QK / M-tiles of PV
+  constexpr int NS = S::kStages;
   constexpr int RBK = row_bytes<FK, D>();
   constexpr int RBV = row_bytes<FV, D>();
 
@@ -113,6 +159,7 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   const int split = t.begin / pps;
   const int wp0 = t.begin + warp * ppw;
   const int wp1 = min(t.begin + t.count, wp0 + ppw);
+  const int n_mt = wp1 > wp0 ? 2 * (wp1 - wp0) : 0;  // the warp's M-tiles (16 keys each)
 
   // ---- Q as the B operand of S^T = K Q^T (heads in N) ----------------------
   uint32_t qf[KS][2];
@@ -148,216 +195,208 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
 
   const uint8_t* kq_base = p.k_quant + (int64_t)g * kPage * RBK;
   const uint8_t* vq_base = p.v_quant + (int64_t)g * kPage * RBV;
-  const uint16_t* ks_base = p.k_scale + (int64_t)g * kPage * NB;
-  const uint16_t* vs_base = p.v_scale + (int64_t)g * kPage * NB;
+  const uint8_t* ks_base = reinterpret_cast<const uint8_t*>(p.k_scale) + (int64_t)g * kPage * NB * 2;
+  const uint8_t* vs_base = reinterpret_cast<const uint8_t*>(p.v_scale) + (int64_t)g * kPage * NB * 2;
   const int64_t kq_page_stride = (int64_t)p.hkv * kPage * RBK;
   const int64_t vq_page_stride = (int64_t)p.hkv * kPage * RBV;
-  const int64_t sc_page_stride = (int64_t)p.hkv * kPage * NB;
+  const int64_t sc_page_stride = (int64_t)p.hkv * kPage * NB * 2;
   const int32_t* pt_row = p.page_table + (int64_t)t.row * p.max_pages;
+  uint8_t* ring = smem + warp * NS * S::kStage;
 
-  for (int pg = wp0; pg < wp1; ++pg) {
-    const int pid = pt_row[pg];
-    if (pid < 0 || pid >= p.num_pages) {
-      if (lane == 0) set_device_error(err, MIXATTN_DEVERR_PAGE_ID);
-      continue;
-    }
-    const uint8_t* kq = kq_base + (int64_t)pid * kq_page_stride;
-    const uint8_t* vq = vq_base + (int64_t)pid * vq_page_stride;
-    const uint16_t* ksc = ks_base + (int64_t)pid * sc_page_stride;
-    const uint16_t* vsc = vs_base + (int64_t)pid * sc_page_stride;
-    const int key0 = pg * kPage;
-
-    // ---------------- S^T = K Q^T for the page's 32 keys ----------------
-    float s[2][4];
+  // Issue the copies of the warp's M-tile i into its stage, then close the group
+  // (an empty group for i past the end keeps the group count uniform).
+  auto issue = [&](int i) {
+    if (i < n_mt) {
+      const int pg = wp0 + (i >> 1), mt = i & 1;
+      const int pid = pt_row[pg];
+      if (pid >= 0 && pid < p.num_pages) {
+        uint8_t* st = ring + (i % NS) * S::kStage;
+        const uint8_t* kq = kq_base + (int64_t)pid * kq_page_stride + 16 * mt * RBK;
+        const uint8_t* vq = vq_base + (int64_t)pid * vq_page_stride + 16 * mt * RBV;
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      const int k_lo = 16 * mt + r, k_hi = k_lo + 8;  // the lane's two key rows
-      s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+        for (int j = lane; j < RBK; j += 32) cp_async16(st + S::kK + swz(16 * j), kq + 16 * j);
+#pragma unroll
+        for (int j = lane; j < RBV; j += 32) cp_async16(st + S::kV + swz(16 * j), vq + 16 * j);
+        constexpr int SC = S::kSc / 16;  // 16-byte chunks of one scale slice
+        if (FK != MIXATTN_KV_F16 && lane < SC)
+          cp_async16(st + S::kKs + 16 * lane, ks_base + (int64_t)pid * sc_page_stride + 16 * mt * NB * 2 + 16 * lane);
+        if (FV != MIXATTN_KV_F16 && lane >= 16 && lane < 16 + SC)
+          cp_async16(st + S::kVs + 16 * (lane - 16),
+                     vs_base + (int64_t)pid * sc_page_stride + 16 * mt * NB * 2 + 16 * (lane - 16));
+      } else if (lane == 0 && (i & 1) == 0) {
+        set_device_error(err, MIXATTN_DEVERR_PAGE_ID);
+      }
+    }
+    cp_async_commit();
+  };
+
+#pragma unroll
+  for (int i = 0; i < NS - 1; ++i) issue(i);
+
+  for (int i = 0; i < n_mt; ++i) {
+    issue(i + NS - 1);      // refills the stage consumed in the previous step
+    cp_async_wait<NS - 1>();  // this lane's copies of M-tile i have landed
+    __syncwarp();             // ... and every other lane's
+    const int pg = wp0 + (i >> 1), mt = i & 1;
+    const int pid = pt_row[pg];
+    if (pid >= 0 && pid < p.num_pages) {
+      const uint8_t* st = ring + (i % NS) * S::kStage;
+      const int key0 = pg * kPage + 16 * mt;  // first key of the M-tile
+
+      // ---------------- S^T = K Q^T for the 16 keys ----------------
+      float s[4] = {0.f, 0.f, 0.f, 0.f};
       float dk_lo[NB], dk_hi[NB];
       if (FK != MIXATTN_KV_F16) {
-        if (NB == 4) {
-          uint2 a = ldg_u64(ksc + k_lo * NB), b2 = ldg_u64(ksc + k_hi * NB);
-          dk_lo[0] = __half2float(__ushort_as_half(a.x & 0xFFFF));
-          dk_lo[1] = __half2float(__ushort_as_half(a.x >> 16));
-          dk_lo[2 % NB] = __half2float(__ushort_as_half(a.y & 0xFFFF));
-          dk_lo[3 % NB] = __half2float(__ushort_as_half(a.y >> 16));
-          dk_hi[0] = __half2float(__ushort_as_half(b2.x & 0xFFFF));
-          dk_hi[1] = __half2float(__ushort_as_half(b2.x >> 16));
-          dk_hi[2 % NB] = __half2float(__ushort_as_half(b2.y & 0xFFFF));
-          dk_hi[3 % NB] = __half2float(__ushort_as_half(b2.y >> 16));
-        } else {
-          uint32_t a = ldg_u32(ksc + k_lo * NB), b2 = ldg_u32(ksc + k_hi * NB);
-          dk_lo[0] = __half2float(__ushort_as_half(a & 0xFFFF));
-          dk_lo[1 % NB] = __half2float(__ushort_as_half(a >> 16));
-          dk_hi[0] = __half2float(__ushort_as_half(b2 & 0xFFFF));
-          dk_hi[1 % NB] = __half2float(__ushort_as_half(b2 >> 16));
-        }
+        load_scales<NB>(st + S::kKs + r * NB * 2, dk_lo);
+        load_scales<NB>(st + S::kKs + (r + 8) * NB * 2, dk_hi);
       }
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
-        uint32_t a0[4], a1[4];  // A fragments of k-steps 2b and 2b+1
+        const uint8_t* kd = st + S::kK;
+        uint32_t a0[4], a1[4];  // A fragments of k-steps 2b and 2b+1 (rows r and r+8)
         if (FK == MIXATTN_KV_Q8_0) {
-          const uint2 wl = ldg_u64(kq + k_lo * RBK + 32 * b + 8 * c);
-          const uint2 wh = ldg_u64(kq + k_hi * RBK + 32 * b + 8 * c);
+          const uint2 wl = lds64(kd + swz(r * RBK + 32 * b + 8 * c));
+          const uint2 wh = lds64(kd + swz((r + 8) * RBK + 32 * b + 8 * c));
           s8x4_to_f16x2x2(wl.x, a0[0], a0[2]);
           s8x4_to_f16x2x2(wh.x, a0[1], a0[3]);
           s8x4_to_f16x2x2(wl.y, a1[0], a1[2]);
           s8x4_to_f16x2x2(wh.y, a1[1], a1[3]);
         } else if (FK == MIXATTN_KV_Q4_0) {
-          const uint32_t yl = ldg_u32(kq + k_lo * RBK + 16 * b + 4 * c);
-          const uint32_t yh = ldg_u32(kq + k_hi * RBK + 16 * b + 4 * c);
+          const uint32_t yl = lds32(kd + swz(r * RBK + 16 * b + 4 * c));
+          const uint32_t yh = lds32(kd + swz((r + 8) * RBK + 16 * b + 4 * c));
           u4x4_to_f16x2x2(yl & 0x0F0F0F0Fu, a0[0], a0[2]);
           u4x4_to_f16x2x2(yh & 0x0F0F0F0Fu, a0[1], a0[3]);
           u4x4_to_f16x2x2((yl >> 4) & 0x0F0F0F0Fu, a1[0], a1[2]);
           u4x4_to_f16x2x2((yh >> 4) & 0x0F0F0F0Fu, a1[1], a1[3]);
         } else {
-          const uint4 wl = ldg_u128(kq + k_lo * RBK + 2 * (32 * b + 8 * c));
-          const uint4 wh = ldg_u128(kq + k_hi * RBK + 2 * (32 * b + 8 * c));
+          const uint4 wl = lds128(kd + swz(r * RBK + 2 * (32 * b + 8 * c)));
+          const uint4 wh = lds128(kd + swz((r + 8) * RBK + 2 * (32 * b + 8 * c)));
           a0[0] = wl.x; a0[1] = wh.x; a0[2] = wl.y; a0[3] = wh.y;
           a1[0] = wl.z; a1[1] = wh.z; a1[2] = wl.w; a1[3] = wh.w;
         }
         if (FK == MIXATTN_KV_F16) {
-          mma_16816(s[mt], a0, qf[2 * b]);
-          mma_16816(s[mt], a1, qf[2 * b + 1]);
+          mma_16816(s, a0, qf[2 * b]);
+          mma_16816(s, a1, qf[2 * b + 1]);
         } else {
           float tmp[4] = {0.f, 0.f, 0.f, 0.f};
           mma_16816(tmp, a0, qf[2 * b]);
           mma_16816(tmp, a1, qf[2 * b + 1]);
-          s[mt][0] = fmaf(dk_lo[b], tmp[0], s[mt][0]);
-          s[mt][1] = fmaf(dk_lo[b], tmp[1], s[mt][1]);
-          s[mt][2] = fmaf(dk_hi[b], tmp[2], s[mt][2]);
-          s[mt][3] = fmaf(dk_hi[b], tmp[3], s[mt][3]);
+          s[0] = fmaf(dk_lo[b], tmp[0], s[0]);
+          s[1] = fmaf(dk_lo[b], tmp[1], s[1]);
+          s[2] = fmaf(dk_hi[b], tmp[2], s[2]);
+          s[3] = fmaf(dk_hi[b], tmp[3], s[3]);
         }
       }
-    }
 
-    // ---------------- online softmax over the page ----------------
-    float pmax[2] = {-CUDART_INF_F, -CUDART_INF_F};
+      // ---------------- online softmax over the 16 keys ----------------
+      const bool v_lo = key0 + r < ri.seq_len, v_hi = key0 + r + 8 < ri.seq_len;
+      s[0] = v_lo ? s[0] * sl2 : -CUDART_INF_F;
+      s[1] = v_lo ? s[1] * sl2 : -CUDART_INF_F;
+      s[2] = v_hi ? s[2] * sl2 : -CUDART_INF_F;
+      s[3] = v_hi ? s[3] * sl2 : -CUDART_INF_F;
+      float pmax[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      const bool v_lo = key0 + 16 * mt + r < ri.seq_len;
-      const bool v_hi = key0 + 16 * mt + r + 8 < ri.seq_len;
-      s[mt][0] = v_lo ? s[mt][0] * sl2 : -CUDART_INF_F;
-      s[mt][1] = v_lo ? s[mt][1] * sl2 : -CUDART_INF_F;
-      s[mt][2] = v_hi ? s[mt][2] * sl2 : -CUDART_INF_F;
-      s[mt][3] = v_hi ? s[mt][3] * sl2 : -CUDART_INF_F;
-      pmax[0] = fmaxf(pmax[0], fmaxf(s[mt][0], s[mt][2]));
-      pmax[1] = fmaxf(pmax[1], fmaxf(s[mt][1], s[mt][3]));
-    }
+      for (int o = 4; o < 32; o <<= 1) {
+        pmax[0] = fmaxf(pmax[0], __shfl_xor_sync(0xFFFFFFFFu, pmax[0], o));
+        pmax[1] = fmaxf(pmax[1], __shfl_xor_sync(0xFFFFFFFFu, pmax[1], o));
+      }
+      float alpha[2];
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      pmax[0] = fmaxf(pmax[0], __shfl_xor_sync(0xFFFFFFFFu, pmax[0], o));
-      pmax[1] = fmaxf(pmax[1], __shfl_xor_sync(0xFFFFFFFFu, pmax[1], o));
-    }
-    float alpha[2];
+      for (int h = 0; h < 2; ++h) {
+        // a fully masked M-tile keeps the running max (its scores are all -inf)
+        const float mn = fmaxf(m_run[h], pmax[h]);
+        alpha[h] = mn == -CUDART_INF_F ? 1.f : ex2(m_run[h] - mn);
+        m_run[h] = mn;
+        l_run[h] *= alpha[h];
+      }
+      const float m0 = m_run[0] == -CUDART_INF_F ? 0.f : m_run[0];
+      const float m1 = m_run[1] == -CUDART_INF_F ? 0.f : m_run[1];
+      s[0] = ex2(s[0] - m0);
+      s[1] = ex2(s[1] - m1);
+      s[2] = ex2(s[2] - m0);
+      s[3] = ex2(s[3] - m1);
+      l_run[0] += s[0] + s[2];
+      l_run[1] += s[1] + s[3];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const float mn = fmaxf(m_run[h], pmax[h]);
-      alpha[h] = ex2(m_run[h] - mn);
-      m_run[h] = mn;
-      l_run[h] *= alpha[h];
-    }
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      s[mt][0] = ex2(s[mt][0] - m_run[0]);
-      s[mt][1] = ex2(s[mt][1] - m_run[1]);
-      s[mt][2] = ex2(s[mt][2] - m_run[0]);
-      s[mt][3] = ex2(s[mt][3] - m_run[1]);
-      l_run[0] += s[mt][0] + s[mt][2];
-      l_run[1] += s[mt][1] + s[mt][3];
-    }
-#pragma unroll
-    for (int i = 0; i < KS; ++i) {
-      o_acc[i][0] *= alpha[0];
-      o_acc[i][1] *= alpha[1];
-      o_acc[i][2] *= alpha[0];
-      o_acc[i][3] *= alpha[1];
-    }
+      for (int i2 = 0; i2 < KS; ++i2) {
+        o_acc[i2][0] *= alpha[0];
+        o_acc[i2][1] *= alpha[1];
+        o_acc[i2][2] *= alpha[0];
+        o_acc[i2][3] *= alpha[1];
+      }
 
-    // ---------------- O^T += V^T P for the page ----------------
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
+      // ---------------- O^T += V^T P for the 16 keys ----------------
       // P (keys x heads) from the S^T fragment layout to the B-operand layout:
       // this lane needs P[key 2c, 2c+1, 2c+8, 2c+9][head r].
       const int src0 = 8 * c + (r >> 1), src1 = src0 + 4;
       float f0[4], f1[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        f0[i] = __shfl_sync(0xFFFFFFFFu, s[mt][i], src0);
-        f1[i] = __shfl_sync(0xFFFFFFFFu, s[mt][i], src1);
+      for (int q = 0; q < 4; ++q) {
+        f0[q] = __shfl_sync(0xFFFFFFFFu, s[q], src0);
+        f1[q] = __shfl_sync(0xFFFFFFFFu, s[q], src1);
       }
       const bool odd = r & 1;
-      const float p0 = odd ? f0[1] : f0[0];   // key 2c
-      const float p1 = odd ? f1[1] : f1[0];   // key 2c+1
-      const float p8 = odd ? f0[3] : f0[2];   // key 2c+8
-      const float p9 = odd ? f1[3] : f1[2];   // key 2c+9
-      const int kk0 = 16 * mt + 2 * c;        // the lane's four keys: kk0, kk0+1, kk0+8, kk0+9
+      const float p0 = odd ? f0[1] : f0[0];  // key 2c
+      const float p1 = odd ? f1[1] : f1[0];  // key 2c+1
+      const float p8 = odd ? f0[3] : f0[2];  // key 2c+8
+      const float p9 = odd ? f1[3] : f1[2];  // key 2c+9
 
-      // V words of the four keys, per block
       uint32_t bfr[NB][2];
       if (FV == MIXATTN_KV_F16) {
         bfr[0][0] = pack_f16x2(p0, p1);
         bfr[0][1] = pack_f16x2(p8, p9);
       } else {
-        float dv[4][NB];
-        const int keys[4] = {kk0, kk0 + 1, kk0 + 8, kk0 + 9};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          if (NB == 4) {
-            uint2 a = ldg_u64(vsc + keys[k] * NB);
-            dv[k][0] = __half2float(__ushort_as_half(a.x & 0xFFFF));
-            dv[k][1] = __half2float(__ushort_as_half(a.x >> 16));
-            dv[k][2 % NB] = __half2float(__ushort_as_half(a.y & 0xFFFF));
-            dv[k][3 % NB] = __half2float(__ushort_as_half(a.y >> 16));
-          } else {
-            uint32_t a = ldg_u32(vsc + keys[k] * NB);
-            dv[k][0] = __half2float(__ushort_as_half(a & 0xFFFF));
-            dv[k][1 % NB] = __half2float(__ushort_as_half(a >> 16));
-          }
-        }
+        float dv0[NB], dv1[NB], dv8[NB], dv9[NB];
+        load_scales<NB>(st + S::kVs + (2 * c) * NB * 2, dv0);
+        load_scales<NB>(st + S::kVs + (2 * c + 1) * NB * 2, dv1);
+        load_scales<NB>(st + S::kVs + (2 * c + 8) * NB * 2, dv8);
+        load_scales<NB>(st + S::kVs + (2 * c + 9) * NB * 2, dv9);
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-          // p == 0 (masked or underflowed) stays 0 whatever the scale holds
-          bfr[b][0] = pack_f16x2(p0 != 0.f ? p0 * dv[0][b] : 0.f, p1 != 0.f ? p1 * dv[1][b] : 0.f);
-          bfr[b][1] = pack_f16x2(p8 != 0.f ? p8 * dv[2][b] : 0.f, p9 != 0.f ? p9 * dv[3][b] : 0.f);
+          // p == 0 (masked or underflowed) stays 0 whatever the scale slot holds
+          bfr[b][0] = pack_f16x2(p0 != 0.f ? p0 * dv0[b] : 0.f, p1 != 0.f ? p1 * dv1[b] : 0.f);
+          bfr[b][1] = pack_f16x2(p8 != 0.f ? p8 * dv8[b] : 0.f, p9 != 0.f ? p9 * dv9[b] : 0.f);
         }
       }
 
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
-        uint32_t a_u0[4], a_u1[4];  // A fragments of M-tiles 2b (u=0) and 2b+1 (u=1)
+        const uint8_t* vd = st + S::kV;
+        uint32_t a_u0[4], a_u1[4];  // A fragments of PV M-tiles 2b (u=0) and 2b+1 (u=1)
         const uint32_t* bb = (FV == MIXATTN_KV_F16) ? bfr[0] : bfr[b];
+        const int kv0 = 2 * c;  // the lane's keys kv0, kv0+1, kv0+8, kv0+9
         if (FV == MIXATTN_KV_Q8_0) {
-          const uint32_t w0 = ldg_u32(vq + (kk0)*RBV + 32 * b + 4 * r);
-          const uint32_t w1 = ldg_u32(vq + (kk0 + 1) * RBV + 32 * b + 4 * r);
-          const uint32_t w8 = ldg_u32(vq + (kk0 + 8) * RBV + 32 * b + 4 * r);
-          const uint32_t w9 = ldg_u32(vq + (kk0 + 9) * RBV + 32 * b + 4 * r);
-          s8x4_to_f16x2x2(prmt(w0, w1, 0x5140u), a_u0[0], a_u0[1]);
-          s8x4_to_f16x2x2(prmt(w8, w9, 0x5140u), a_u0[2], a_u0[3]);
-          s8x4_to_f16x2x2(prmt(w0, w1, 0x7362u), a_u1[0], a_u1[1]);
-          s8x4_to_f16x2x2(prmt(w8, w9, 0x7362u), a_u1[2], a_u1[3]);
+          uint4 w;
+          w.x = lds32(vd + swz(kv0 * RBV + 32 * b + 4 * r));
+          w.y = lds32(vd + swz((kv0 + 1) * RBV + 32 * b + 4 * r));
+          w.z = lds32(vd + swz((kv0 + 8) * RBV + 32 * b + 4 * r));
+          w.w = lds32(vd + swz((kv0 + 9) * RBV + 32 * b + 4 * r));
+          s8x4_to_f16x2x2(prmt(w.x, w.y, 0x5140u), a_u0[0], a_u0[1]);
+          s8x4_to_f16x2x2(prmt(w.z, w.w, 0x5140u), a_u0[2], a_u0[3]);
+          s8x4_to_f16x2x2(prmt(w.x, w.y, 0x7362u), a_u1[0], a_u1[1]);
+          s8x4_to_f16x2x2(prmt(w.z, w.w, 0x7362u), a_u1[2], a_u1[3]);
         } else if (FV == MIXATTN_KV_Q4_0) {
-          const uint32_t h0 = ldg_u16(vq + (kk0)*RBV + 16 * b + 2 * r);
-          const uint32_t h1 = ldg_u16(vq + (kk0 + 1) * RBV + 16 * b + 2 * r);
-          const uint32_t h8 = ldg_u16(vq + (kk0 + 8) * RBV + 16 * b + 2 * r);
-          const uint32_t h9 = ldg_u16(vq + (kk0 + 9) * RBV + 16 * b + 2 * r);
-          const uint32_t x01 = prmt(h0, h1, 0x5140u), x89 = prmt(h8, h9, 0x5140u);
+          // the 4 bytes holding the lane's 2 bytes (block bytes 2r, 2r+1) at half (r & 1)
+          uint4 w;
+          w.x = lds32(vd + swz(kv0 * RBV + 16 * b + 4 * (r >> 1)));
+          w.y = lds32(vd + swz((kv0 + 1) * RBV + 16 * b + 4 * (r >> 1)));
+          w.z = lds32(vd + swz((kv0 + 8) * RBV + 16 * b + 4 * (r >> 1)));
+          w.w = lds32(vd + swz((kv0 + 9) * RBV + 16 * b + 4 * (r >> 1)));
+          const uint32_t sel = (r & 1) ? 0x7362u : 0x5140u;
+          const uint32_t x01 = prmt(w.x, w.y, sel), x89 = prmt(w.z, w.w, sel);
           u4x4_to_f16x2x2(x01 & 0x0F0F0F0Fu, a_u0[0], a_u0[1]);
           u4x4_to_f16x2x2(x89 & 0x0F0F0F0Fu, a_u0[2], a_u0[3]);
           u4x4_to_f16x2x2((x01 >> 4) & 0x0F0F0F0Fu, a_u1[0], a_u1[1]);
           u4x4_to_f16x2x2((x89 >> 4) & 0x0F0F0F0Fu, a_u1[2], a_u1[3]);
         } else {
           // fp16 values: zero the words of keys past the row so stale data never reaches the MMA
-          const bool v0 = key0 + kk0 < ri.seq_len, v1 = key0 + kk0 + 1 < ri.seq_len;
-          const bool v8 = key0 + kk0 + 8 < ri.seq_len, v9 = key0 + kk0 + 9 < ri.seq_len;
-          uint2 e0 = ldg_u64(vq + (kk0)*RBV + 2 * (32 * b + 4 * r));
-          uint2 e1 = ldg_u64(vq + (kk0 + 1) * RBV + 2 * (32 * b + 4 * r));
-          uint2 e8 = ldg_u64(vq + (kk0 + 8) * RBV + 2 * (32 * b + 4 * r));
-          uint2 e9 = ldg_u64(vq + (kk0 + 9) * RBV + 2 * (32 * b + 4 * r));
-          if (!v0) e0 = make_uint2(0u, 0u);
-          if (!v1) e1 = make_uint2(0u, 0u);
-          if (!v8) e8 = make_uint2(0u, 0u);
-          if (!v9) e9 = make_uint2(0u, 0u);
+          const bool ok0 = key0 + 2 * c < ri.seq_len, ok1 = key0 + 2 * c + 1 < ri.seq_len;
+          const bool ok8 = key0 + 2 * c + 8 < ri.seq_len, ok9 = key0 + 2 * c + 9 < ri.seq_len;
+          const int vo = 2 * (32 * b + 4 * r);
+          const uint2 e0 = ok0 ? lds64(vd + swz(kv0 * RBV + vo)) : make_uint2(0u, 0u);
+          const uint2 e1 = ok1 ? lds64(vd + swz((kv0 + 1) * RBV + vo)) : make_uint2(0u, 0u);
+          const uint2 e8 = ok8 ? lds64(vd + swz((kv0 + 8) * RBV + vo)) : make_uint2(0u, 0u);
+          const uint2 e9 = ok9 ? lds64(vd + swz((kv0 + 9) * RBV + vo)) : make_uint2(0u, 0u);
           a_u0[0] = prmt(e0.x, e1.x, 0x5410u);
           a_u0[1] = prmt(e0.x, e1.x, 0x7632u);
           a_u0[2] = prmt(e8.x, e9.x, 0x5410u);
@@ -372,7 +411,9 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
         mma_16816(o_acc[2 * b + 1], a_u1, bop);
       }
     }
+    __syncwarp();  // every lane is done with this stage before it is refilled
   }
+  cp_async_wait<0>();
 
   // ---------------- warp partial -> shared memory ----------------
 #pragma unroll
@@ -380,8 +421,9 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
     l_run[0] += __shfl_xor_sync(0xFFFFFFFFu, l_run[0], o);
     l_run[1] += __shfl_xor_sync(0xFFFFFFFFu, l_run[1], o);
   }
+  __syncthreads();  // the staging rings are no longer needed: reuse them as merge scratch
   float* ws = reinterpret_cast<float*>(smem);
-  float* wm = ws + warp * DecodeSmem<D>::kPerWarp;  // m[8], l[8], O[8][D]
+  float* wm = ws + warp * S::kPerWarp;  // m[8], l[8], O[8][D]
   const int h0 = 2 * c, h1 = 2 * c + 1;
   if (r == 0) {
     if (h0 < G) { wm[h0] = m_run[0]; wm[8 + h0] = l_run[0]; }
@@ -409,11 +451,11 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   for (int idx = tid; idx < n_out; idx += kThreads) {
     const int h = idx / D, d = idx - h * D;
     float mmax = -CUDART_INF_F;
-    for (int w = 0; w < n_warps_used; ++w) mmax = fmaxf(mmax, ws[w * DecodeSmem<D>::kPerWarp + h]);
+    for (int w = 0; w < n_warps_used; ++w) mmax = fmaxf(mmax, ws[w * S::kPerWarp + h]);
     float lsum = 0.f, osum = 0.f;
     for (int w = 0; w < n_warps_used; ++w) {
-      const float* x = ws + w * DecodeSmem<D>::kPerWarp;
-      const float sc = ex2(x[h] - mmax);
+      const float* x = ws + w * S::kPerWarp;
+      const float sc = x[h] == -CUDART_INF_F ? 0.f : ex2(x[h] - mmax);
       lsum += sc * x[8 + h];
       osum += sc * x[16 + h * D + d];
     }
@@ -453,7 +495,8 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
     float lsum = 0.f, osum = 0.f;
     for (int s2 = 0; s2 < ns; ++s2) {
       const float* x = p.partials + (int64_t)(first + s2) * G * (D + 2);
-      const float sc = ex2(__ldcg(x + G * D + 2 * h) - mmax);
+      const float mx = __ldcg(x + G * D + 2 * h);
+      const float sc = mx == -CUDART_INF_F ? 0.f : ex2(mx - mmax);
       lsum += sc * __ldcg(x + G * D + 2 * h + 1);
       osum += sc * __ldcg(x + h * D + d);
     }
@@ -804,20 +847,24 @@ template <int FK, int FV, int D>
 cudaError_t launch_attention_t(const AttnParams& p, unsigned int* err, cudaStream_t s) {
   const int n_tiles = p.n_chunk_tiles + p.n_decode_tiles;
   if (n_tiles == 0) return cudaSuccess;
-  if (p.n_chunk_tiles == 0) {
-    const size_t sm = DecodeSmem<D>::kTotal;
-    decode_attention_kernel<FK, FV, D><<<p.n_decode_tiles, kThreads, sm, s>>>(p, err);
-    return cudaGetLastError();
-  }
-  const size_t sm = ChunkSmem<FK, FV, D>::kTotal;
-  static bool configured = false;  // per process; the attribute is per function
+  constexpr int kDec = DecodeSmem<FK, FV, D>::kTotal;
+  constexpr int kChunk = ChunkSmem<FK, FV, D>::kTotal;
+  constexpr int kFused = kDec > kChunk ? kDec : kChunk;
+  static bool configured = false;  // the attribute is per function, once per process
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(mixed_attention_kernel<FK, FV, D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    cudaError_t e = cudaFuncSetAttribute(decode_attention_kernel<FK, FV, D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kDec);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mixed_attention_kernel<FK, FV, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kFused);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  mixed_attention_kernel<FK, FV, D><<<n_tiles, kThreads, sm, s>>>(p, err);
+  if (p.n_chunk_tiles == 0) {
+    decode_attention_kernel<FK, FV, D><<<p.n_decode_tiles, kThreads, kDec, s>>>(p, err);
+  } else {
+    mixed_attention_kernel<FK, FV, D><<<n_tiles, kThreads, kFused, s>>>(p, err);
+  }
   return cudaGetLastError();
 }
 
