@@ -220,6 +220,37 @@ int mixattn_workspace_bytes(const mixattn_kv_cache* cache, int32_t num_q_heads, 
                             const int32_t* row_kinds, const int32_t* seq_lens,
                             const int32_t* q_offsets, int32_t max_pages, size_t* workspace_bytes);
 
+/*
+ * The same attention step with no allocation of any kind.  The reference pages
+ * have no counterpart of this entry point; it exists for callers that cannot
+ * give the library a device workspace: a host runtime that reserves all GPU
+ * memory up front and forbids further cudaMalloc calls, a latency-critical
+ * serving loop where a device allocation would synchronise the device, or a
+ * plain C host with no allocator for device buffers.
+ *
+ * Arguments are those of mixattn_mixed_attention minus the workspace: the
+ * workspace lives in a library-owned file-scope device array of 16 MiB, which
+ * every GPU that loads the library holds until the process exits, and the tile
+ * list is staged in a library-owned host array.  No cudaMalloc, cudaFree,
+ * cudaHostAlloc or other allocating routine is called.
+ *   - A batch whose workspace (mixattn_workspace_bytes) exceeds 16 MiB -- at
+ *     head_dim 128 and 4 q heads per kv head, about 8000 decode split tiles --
+ *     returns MIXATTN_ERR_WORKSPACE and launches nothing.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any stream
+ *     capture.
+ *   - All calls share the one array, which keeps the previous call's contents;
+ *     each call re-zeroes what must start at zero (the split counters).  Calls
+ *     whose GPU work overlaps -- on two streams, or from host threads without
+ *     ordering -- race on the array.
+ *   - The tile list is copied from pageable host memory, so the call waits for
+ *     the stream's earlier work before it returns.
+ */
+int mixattn_mixed_attention_noalloc(const mixattn_kv_cache* cache, int32_t num_q_heads, const void* q,
+                                    const int32_t* page_table, int32_t max_pages, int32_t n_rows,
+                                    const int32_t* seq_lens, const int32_t* q_offsets,
+                                    const int32_t* row_kinds, void* o, mixattn_stream stream);
+
 /* Synchronously read (and, if clear != 0, reset) the device error word of the
  * current device: an OR of MIXATTN_DEVERR_* bits set by kernels since the
  * last clear.  Returns the word, or a negative status. */

@@ -32,6 +32,7 @@ EXPORTED = [
     "mixattn_plan_create", "mixattn_plan_update", "mixattn_plan_info", "mixattn_run",
     "mixattn_plan_destroy", "mixattn_mixed_attention", "mixattn_workspace_bytes",
     "mixattn_device_error", "mixattn_status_string", "mixattn_version",
+    "mixattn_mixed_attention_noalloc",
 ]
 
 
@@ -87,6 +88,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.mixattn_plan_destroy.restype = None
     lib.mixattn_mixed_attention.argtypes = [cachep, i32, vp, vp, i32, i32, i32p, i32p, i32p, vp, vp, sz, vp]
     lib.mixattn_mixed_attention.restype = ctypes.c_int
+    lib.mixattn_mixed_attention_noalloc.argtypes = [cachep, i32, vp, vp, i32, i32, i32p, i32p, i32p, vp, vp]
+    lib.mixattn_mixed_attention_noalloc.restype = ctypes.c_int
     lib.mixattn_workspace_bytes.argtypes = [cachep, i32, i32, i32p, i32p, i32p, i32, ctypes.POINTER(sz)]
     lib.mixattn_workspace_bytes.restype = ctypes.c_int
     lib.mixattn_device_error.argtypes = [i32]
@@ -292,6 +295,23 @@ def mixed_attention(cache: KVCache, q, page_table, seq_lens, q_offsets, row_kind
         _i32_array(seq_lens), _i32_array(q_offsets), _i32_array(row_kinds), _ptr(o), _ptr(workspace),
         int(workspace.numel()), _stream_handle(stream))
     _check(st, "mixattn_mixed_attention")
+    return o
+
+
+def mixed_attention_noalloc(cache: KVCache, q, page_table, seq_lens, q_offsets, row_kinds, o=None,
+                            stream=None):
+    """Same step with the workspace held by the library (nothing is allocated
+    by the call): for callers that cannot provide device scratch memory.
+    Batches needing more than the library's 16 MiB of scratch raise
+    MixattnError(ERR_WORKSPACE); overlapping calls on different streams race."""
+    import torch
+    if o is None:
+        o = torch.empty_like(q)
+    st = load().mixattn_mixed_attention_noalloc(
+        ctypes.byref(cache.desc()), int(q.shape[1]), _ptr(q), _ptr(page_table), int(page_table.shape[1]),
+        len(seq_lens), _i32_array(seq_lens), _i32_array(q_offsets), _i32_array(row_kinds), _ptr(o),
+        _stream_handle(stream))
+    _check(st, "mixattn_mixed_attention_noalloc")
     return o
 
 

@@ -165,6 +165,10 @@ int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* k
 }
 
 }  // namespace
+
+// Address of this device's error word, for launchers in other translation units.
+unsigned int* device_error_address() { return error_word(); }
+
 }  // namespace mixattn
 
 using namespace mixattn;
