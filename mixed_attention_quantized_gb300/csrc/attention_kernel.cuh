@@ -85,14 +85,20 @@ struct DecodeSmem {
   static constexpr int kKs = kV + 16 * kRbV;
   static constexpr int kVs = kKs + (FK == MIXATTN_KV_F16 ? 0 : kSc);
   static constexpr int kStage = (kVs + (FV == MIXATTN_KV_F16 ? 0 : kSc) + 127) / 128 * 128;
-  static constexpr int kBudget = 212 * 1024;
-  static constexpr int kStagesRaw = kBudget / (kWarps * kStage);
-  static constexpr int kStages = kStagesRaw > 8 ? 8 : (kStagesRaw < 2 ? 2 : kStagesRaw);
-  static constexpr int kRing = kWarps * kStages * kStage;
+  static constexpr int stages_for(int budget) {
+    return budget / (kWarps * kStage) > 8 ? 8 : (budget / (kWarps * kStage) < 2 ? 2 : budget / (kWarps * kStage));
+  }
   // after the page loop the same memory holds the warp partials: m[8], l[8], O[8][D]
   static constexpr int kPerWarp = 16 + kMaxGroup * D;
   static constexpr int kMerge = kWarps * kPerWarp * 4;
-  static constexpr int kTotal = (kRing > kMerge ? kRing : kMerge) + 16;
+  static constexpr int total(int ns) { return (kWarps * ns * kStage > kMerge ? kWarps * ns * kStage : kMerge) + 16; }
+  // decode-only launches: two CTAs per SM when two stages per warp fit in ~106 KB,
+  // else one CTA per SM with a deeper ring
+  static constexpr int kPairBudget = 106 * 1024;
+  static constexpr bool kTwoPerSm = kWarps * 2 * kStage <= kPairBudget;
+  static constexpr int kSoloStages = stages_for(kTwoPerSm ? kPairBudget : 212 * 1024);
+  static constexpr int kSoloMinBlocks = kTwoPerSm ? 2 : 1;
+  static constexpr int kTotal = total(kSoloStages);
   static_assert(kTotal <= 227 * 1024, "decode staging does not fit in shared memory");
 };
 
@@ -138,13 +144,12 @@ __device__ __forceinline__ void load_scales(const uint8_t* p, float (&out)[NB]) 
   }
 }
 
-template <int FK, int FV, int D>
+template <int FK, int FV, int D, int NS>
 __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc& t, int dec_idx, uint8_t* smem,
                                             unsigned int* err) {
   using S = DecodeSmem<FK, FV, D>;
   constexpr int NB = D / kBlock;   // scale blocks per row
   constexpr int KS = D / 16;       // k-steps of QK / M-tiles of PV
-  constexpr int NS = S::kStages;
   constexpr int RBK = row_bytes<FK, D>();
   constexpr int RBV = row_bytes<FV, D>();
 
@@ -161,8 +166,10 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   const int wp1 = min(t.begin + t.count, wp0 + ppw);
   const int n_mt = wp1 > wp0 ? 2 * (wp1 - wp0) : 0;  // the warp's M-tiles (16 keys each)
 
-  // ---- Q as the B operand of S^T = K Q^T (heads in N) ----------------------
-  uint32_t qf[KS][2];
+  // ---- Q as the A operand of S = Q K^T: head r in M row r (rows 8..15 zero) ----
+  // k-slots 2c,2c+1 | 2c+8,2c+9 of k-step 2b+hs hold head dims
+  //   Q8_0 / fp16: 32b+8c+4hs + {0,1 | 2,3};   Q4_0: 32b+16hs+4c + {0,1 | 2,3}
+  uint32_t qa[KS][2];
   {
     const bool real = r < G;
     const uint16_t* qrow =
@@ -172,16 +179,16 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
       if (FK == MIXATTN_KV_Q4_0) {
         uint2 lo = real ? ldg_u64(qrow + 32 * b + 4 * c) : make_uint2(0u, 0u);
         uint2 hi = real ? ldg_u64(qrow + 32 * b + 16 + 4 * c) : make_uint2(0u, 0u);
-        qf[2 * b][0] = lo.x;
-        qf[2 * b][1] = lo.y;
-        qf[2 * b + 1][0] = hi.x;
-        qf[2 * b + 1][1] = hi.y;
+        qa[2 * b][0] = lo.x;
+        qa[2 * b][1] = lo.y;
+        qa[2 * b + 1][0] = hi.x;
+        qa[2 * b + 1][1] = hi.y;
       } else {
         uint4 v = real ? ldg_u128(qrow + 32 * b + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
-        qf[2 * b][0] = v.x;
-        qf[2 * b][1] = v.y;
-        qf[2 * b + 1][0] = v.z;
-        qf[2 * b + 1][1] = v.w;
+        qa[2 * b][0] = v.x;
+        qa[2 * b][1] = v.y;
+        qa[2 * b + 1][0] = v.z;
+        qa[2 * b + 1][1] = v.w;
       }
     }
   }
@@ -189,8 +196,7 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   float o_acc[KS][4];
 #pragma unroll
   for (int i = 0; i < KS; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
-  float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F};
-  float l_run[2] = {0.f, 0.f};
+  float m_run = -CUDART_INF_F, l_run = 0.f;  // head r
   const float sl2 = p.scale_log2;
 
   const uint8_t* kq_base = p.k_quant + (int64_t)g * kPage * RBK;
@@ -233,8 +239,9 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
 #pragma unroll
   for (int i = 0; i < NS - 1; ++i) issue(i);
 
+  const int kv0 = 2 * c;  // the lane's keys in an M-tile: kv0, kv0+1 (n-tile 0), kv0+8, kv0+9 (n-tile 1)
   for (int i = 0; i < n_mt; ++i) {
-    issue(i + NS - 1);      // refills the stage consumed in the previous step
+    issue(i + NS - 1);        // refills the stage consumed in the previous step
     cp_async_wait<NS - 1>();  // this lane's copies of M-tile i have landed
     __syncwarp();             // ... and every other lane's
     const int pg = wp0 + (i >> 1), mt = i & 1;
@@ -242,120 +249,119 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
     if (pid >= 0 && pid < p.num_pages) {
       const uint8_t* st = ring + (i % NS) * S::kStage;
       const int key0 = pg * kPage + 16 * mt;  // first key of the M-tile
+      const bool partial = key0 + 16 > ri.seq_len;
 
-      // ---------------- S^T = K Q^T for the 16 keys ----------------
+      // ---------------- S = Q K^T: head r x keys kv0, kv0+1, kv0+8, kv0+9 ----------------
       float s[4] = {0.f, 0.f, 0.f, 0.f};
-      float dk_lo[NB], dk_hi[NB];
+      float dk0[NB], dk1[NB], dk8[NB], dk9[NB];
       if (FK != MIXATTN_KV_F16) {
-        load_scales<NB>(st + S::kKs + r * NB * 2, dk_lo);
-        load_scales<NB>(st + S::kKs + (r + 8) * NB * 2, dk_hi);
+        load_scales<NB>(st + S::kKs + kv0 * NB * 2, dk0);
+        load_scales<NB>(st + S::kKs + (kv0 + 1) * NB * 2, dk1);
+        load_scales<NB>(st + S::kKs + (kv0 + 8) * NB * 2, dk8);
+        load_scales<NB>(st + S::kKs + (kv0 + 9) * NB * 2, dk9);
       }
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         const uint8_t* kd = st + S::kK;
-        uint32_t a0[4], a1[4];  // A fragments of k-steps 2b and 2b+1 (rows r and r+8)
+        uint32_t b0[2][2], b1[2][2];  // B fragments [n-tile][reg] of k-steps 2b and 2b+1 (keys r, r+8)
         if (FK == MIXATTN_KV_Q8_0) {
           const uint2 wl = lds64(kd + swz(r * RBK + 32 * b + 8 * c));
           const uint2 wh = lds64(kd + swz((r + 8) * RBK + 32 * b + 8 * c));
-          s8x4_to_f16x2x2(wl.x, a0[0], a0[2]);
-          s8x4_to_f16x2x2(wh.x, a0[1], a0[3]);
-          s8x4_to_f16x2x2(wl.y, a1[0], a1[2]);
-          s8x4_to_f16x2x2(wh.y, a1[1], a1[3]);
+          s8x4_to_f16x2x2(wl.x, b0[0][0], b0[0][1]);
+          s8x4_to_f16x2x2(wh.x, b0[1][0], b0[1][1]);
+          s8x4_to_f16x2x2(wl.y, b1[0][0], b1[0][1]);
+          s8x4_to_f16x2x2(wh.y, b1[1][0], b1[1][1]);
         } else if (FK == MIXATTN_KV_Q4_0) {
           const uint32_t yl = lds32(kd + swz(r * RBK + 16 * b + 4 * c));
           const uint32_t yh = lds32(kd + swz((r + 8) * RBK + 16 * b + 4 * c));
-          u4x4_to_f16x2x2(yl & 0x0F0F0F0Fu, a0[0], a0[2]);
-          u4x4_to_f16x2x2(yh & 0x0F0F0F0Fu, a0[1], a0[3]);
-          u4x4_to_f16x2x2((yl >> 4) & 0x0F0F0F0Fu, a1[0], a1[2]);
-          u4x4_to_f16x2x2((yh >> 4) & 0x0F0F0F0Fu, a1[1], a1[3]);
+          u4x4_to_f16x2x2(yl & 0x0F0F0F0Fu, b0[0][0], b0[0][1]);
+          u4x4_to_f16x2x2(yh & 0x0F0F0F0Fu, b0[1][0], b0[1][1]);
+          u4x4_to_f16x2x2((yl >> 4) & 0x0F0F0F0Fu, b1[0][0], b1[0][1]);
+          u4x4_to_f16x2x2((yh >> 4) & 0x0F0F0F0Fu, b1[1][0], b1[1][1]);
         } else {
           const uint4 wl = lds128(kd + swz(r * RBK + 2 * (32 * b + 8 * c)));
           const uint4 wh = lds128(kd + swz((r + 8) * RBK + 2 * (32 * b + 8 * c)));
-          a0[0] = wl.x; a0[1] = wh.x; a0[2] = wl.y; a0[3] = wh.y;
-          a1[0] = wl.z; a1[1] = wh.z; a1[2] = wl.w; a1[3] = wh.w;
+          b0[0][0] = wl.x; b0[0][1] = wl.y; b0[1][0] = wh.x; b0[1][1] = wh.y;
+          b1[0][0] = wl.z; b1[0][1] = wl.w; b1[1][0] = wh.z; b1[1][1] = wh.w;
         }
+        const uint32_t a0[4] = {qa[2 * b][0], 0u, qa[2 * b][1], 0u};
+        const uint32_t a1[4] = {qa[2 * b + 1][0], 0u, qa[2 * b + 1][1], 0u};
         if (FK == MIXATTN_KV_F16) {
-          mma_16816(s, a0, qf[2 * b]);
-          mma_16816(s, a1, qf[2 * b + 1]);
+          float u0[4], u1[4];
+          mma_16816_c(u0, a0, b0[0], s[0], s[1], 0.f, 0.f);
+          mma_16816(u0, a1, b1[0]);
+          mma_16816_c(u1, a0, b0[1], s[2], s[3], 0.f, 0.f);
+          mma_16816(u1, a1, b1[1]);
+          s[0] = u0[0]; s[1] = u0[1]; s[2] = u1[0]; s[3] = u1[1];
         } else {
-          float tmp[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_16816(tmp, a0, qf[2 * b]);
-          mma_16816(tmp, a1, qf[2 * b + 1]);
-          s[0] = fmaf(dk_lo[b], tmp[0], s[0]);
-          s[1] = fmaf(dk_lo[b], tmp[1], s[1]);
-          s[2] = fmaf(dk_hi[b], tmp[2], s[2]);
-          s[3] = fmaf(dk_hi[b], tmp[3], s[3]);
+          float u0[4], u1[4];  // per-block dot products of exact integer codes
+          mma_16816_c(u0, a0, b0[0], 0.f, 0.f, 0.f, 0.f);
+          mma_16816(u0, a1, b1[0]);
+          mma_16816_c(u1, a0, b0[1], 0.f, 0.f, 0.f, 0.f);
+          mma_16816(u1, a1, b1[1]);
+          s[0] = fmaf(dk0[b], u0[0], s[0]);
+          s[1] = fmaf(dk1[b], u0[1], s[1]);
+          s[2] = fmaf(dk8[b], u1[0], s[2]);
+          s[3] = fmaf(dk9[b], u1[1], s[3]);
         }
       }
 
-      // ---------------- online softmax over the 16 keys ----------------
-      const bool v_lo = key0 + r < ri.seq_len, v_hi = key0 + r + 8 < ri.seq_len;
-      s[0] = v_lo ? s[0] * sl2 : -CUDART_INF_F;
-      s[1] = v_lo ? s[1] * sl2 : -CUDART_INF_F;
-      s[2] = v_hi ? s[2] * sl2 : -CUDART_INF_F;
-      s[3] = v_hi ? s[3] * sl2 : -CUDART_INF_F;
-      float pmax[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        pmax[0] = fmaxf(pmax[0], __shfl_xor_sync(0xFFFFFFFFu, pmax[0], o));
-        pmax[1] = fmaxf(pmax[1], __shfl_xor_sync(0xFFFFFFFFu, pmax[1], o));
+      // ---------------- online softmax over the 16 keys (head r) ----------------
+      s[0] = key0 + kv0 < ri.seq_len ? s[0] * sl2 : -CUDART_INF_F;
+      s[1] = key0 + kv0 + 1 < ri.seq_len ? s[1] * sl2 : -CUDART_INF_F;
+      s[2] = key0 + kv0 + 8 < ri.seq_len ? s[2] * sl2 : -CUDART_INF_F;
+      s[3] = key0 + kv0 + 9 < ri.seq_len ? s[3] * sl2 : -CUDART_INF_F;
+      float pm = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+      pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 1));
+      pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 2));
+      // exact running max: the largest weight is exactly 1, so its fp16 P' is exact
+      float alpha = 1.f;
+      if (pm > m_run) {  // also the first M-tile with a valid key (m_run = -inf)
+        alpha = ex2(m_run - pm);
+        m_run = pm;
       }
-      float alpha[2];
+      const float mref = m_run == -CUDART_INF_F ? 0.f : m_run;
+      const float p0 = ex2(s[0] - mref), p1 = ex2(s[1] - mref);
+      const float p8 = ex2(s[2] - mref), p9 = ex2(s[3] - mref);
+      l_run = l_run * alpha + ((p0 + p1) + (p8 + p9));
+      if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+        // O columns are heads 2c, 2c+1: their factors live in lanes 8c and 8c+4
+        const float a_even = __shfl_sync(0xFFFFFFFFu, alpha, 8 * c);
+        const float a_odd = __shfl_sync(0xFFFFFFFFu, alpha, 8 * c + 4);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        // a fully masked M-tile keeps the running max (its scores are all -inf)
-        const float mn = fmaxf(m_run[h], pmax[h]);
-        alpha[h] = mn == -CUDART_INF_F ? 1.f : ex2(m_run[h] - mn);
-        m_run[h] = mn;
-        l_run[h] *= alpha[h];
-      }
-      const float m0 = m_run[0] == -CUDART_INF_F ? 0.f : m_run[0];
-      const float m1 = m_run[1] == -CUDART_INF_F ? 0.f : m_run[1];
-      s[0] = ex2(s[0] - m0);
-      s[1] = ex2(s[1] - m1);
-      s[2] = ex2(s[2] - m0);
-      s[3] = ex2(s[3] - m1);
-      l_run[0] += s[0] + s[2];
-      l_run[1] += s[1] + s[3];
-#pragma unroll
-      for (int i2 = 0; i2 < KS; ++i2) {
-        o_acc[i2][0] *= alpha[0];
-        o_acc[i2][1] *= alpha[1];
-        o_acc[i2][2] *= alpha[0];
-        o_acc[i2][3] *= alpha[1];
+        for (int i2 = 0; i2 < KS; ++i2) {
+          o_acc[i2][0] *= a_even;
+          o_acc[i2][1] *= a_odd;
+          o_acc[i2][2] *= a_even;
+          o_acc[i2][3] *= a_odd;
+        }
       }
 
       // ---------------- O^T += V^T P for the 16 keys ----------------
-      // P (keys x heads) from the S^T fragment layout to the B-operand layout:
-      // this lane needs P[key 2c, 2c+1, 2c+8, 2c+9][head r].
-      const int src0 = 8 * c + (r >> 1), src1 = src0 + 4;
-      float f0[4], f1[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        f0[q] = __shfl_sync(0xFFFFFFFFu, s[q], src0);
-        f1[q] = __shfl_sync(0xFFFFFFFFu, s[q], src1);
-      }
-      const bool odd = r & 1;
-      const float p0 = odd ? f0[1] : f0[0];  // key 2c
-      const float p1 = odd ? f1[1] : f1[0];  // key 2c+1
-      const float p8 = odd ? f0[3] : f0[2];  // key 2c+8
-      const float p9 = odd ? f1[3] : f1[2];  // key 2c+9
-
+      // P is already in the B-operand layout: this lane holds P[key kv0.., kv0+9][head r].
       uint32_t bfr[NB][2];
       if (FV == MIXATTN_KV_F16) {
         bfr[0][0] = pack_f16x2(p0, p1);
         bfr[0][1] = pack_f16x2(p8, p9);
       } else {
         float dv0[NB], dv1[NB], dv8[NB], dv9[NB];
-        load_scales<NB>(st + S::kVs + (2 * c) * NB * 2, dv0);
-        load_scales<NB>(st + S::kVs + (2 * c + 1) * NB * 2, dv1);
-        load_scales<NB>(st + S::kVs + (2 * c + 8) * NB * 2, dv8);
-        load_scales<NB>(st + S::kVs + (2 * c + 9) * NB * 2, dv9);
+        load_scales<NB>(st + S::kVs + kv0 * NB * 2, dv0);
+        load_scales<NB>(st + S::kVs + (kv0 + 1) * NB * 2, dv1);
+        load_scales<NB>(st + S::kVs + (kv0 + 8) * NB * 2, dv8);
+        load_scales<NB>(st + S::kVs + (kv0 + 9) * NB * 2, dv9);
+        if (partial) {
+          // p == 0 (a key past the row) stays 0 whatever its scale slot holds
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          // p == 0 (masked or underflowed) stays 0 whatever the scale slot holds
-          bfr[b][0] = pack_f16x2(p0 != 0.f ? p0 * dv0[b] : 0.f, p1 != 0.f ? p1 * dv1[b] : 0.f);
-          bfr[b][1] = pack_f16x2(p8 != 0.f ? p8 * dv8[b] : 0.f, p9 != 0.f ? p9 * dv9[b] : 0.f);
+          for (int b = 0; b < NB; ++b) {
+            bfr[b][0] = pack_f16x2(p0 != 0.f ? p0 * dv0[b] : 0.f, p1 != 0.f ? p1 * dv1[b] : 0.f);
+            bfr[b][1] = pack_f16x2(p8 != 0.f ? p8 * dv8[b] : 0.f, p9 != 0.f ? p9 * dv9[b] : 0.f);
+          }
+        } else {
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            bfr[b][0] = pack_f16x2(p0 * dv0[b], p1 * dv1[b]);
+            bfr[b][1] = pack_f16x2(p8 * dv8[b], p9 * dv9[b]);
+          }
         }
       }
 
@@ -364,7 +370,6 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
         const uint8_t* vd = st + S::kV;
         uint32_t a_u0[4], a_u1[4];  // A fragments of PV M-tiles 2b (u=0) and 2b+1 (u=1)
         const uint32_t* bb = (FV == MIXATTN_KV_F16) ? bfr[0] : bfr[b];
-        const int kv0 = 2 * c;  // the lane's keys kv0, kv0+1, kv0+8, kv0+9
         if (FV == MIXATTN_KV_Q8_0) {
           uint4 w;
           w.x = lds32(vd + swz(kv0 * RBV + 32 * b + 4 * r));
@@ -390,8 +395,8 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
           u4x4_to_f16x2x2((x89 >> 4) & 0x0F0F0F0Fu, a_u1[2], a_u1[3]);
         } else {
           // fp16 values: zero the words of keys past the row so stale data never reaches the MMA
-          const bool ok0 = key0 + 2 * c < ri.seq_len, ok1 = key0 + 2 * c + 1 < ri.seq_len;
-          const bool ok8 = key0 + 2 * c + 8 < ri.seq_len, ok9 = key0 + 2 * c + 9 < ri.seq_len;
+          const bool ok0 = key0 + kv0 < ri.seq_len, ok1 = key0 + kv0 + 1 < ri.seq_len;
+          const bool ok8 = key0 + kv0 + 8 < ri.seq_len, ok9 = key0 + kv0 + 9 < ri.seq_len;
           const int vo = 2 * (32 * b + 4 * r);
           const uint2 e0 = ok0 ? lds64(vd + swz(kv0 * RBV + vo)) : make_uint2(0u, 0u);
           const uint2 e1 = ok1 ? lds64(vd + swz((kv0 + 1) * RBV + vo)) : make_uint2(0u, 0u);
@@ -416,18 +421,15 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   cp_async_wait<0>();
 
   // ---------------- warp partial -> shared memory ----------------
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    l_run[0] += __shfl_xor_sync(0xFFFFFFFFu, l_run[0], o);
-    l_run[1] += __shfl_xor_sync(0xFFFFFFFFu, l_run[1], o);
-  }
+  l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 1);
+  l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 2);
   __syncthreads();  // the staging rings are no longer needed: reuse them as merge scratch
   float* ws = reinterpret_cast<float*>(smem);
   float* wm = ws + warp * S::kPerWarp;  // m[8], l[8], O[8][D]
   const int h0 = 2 * c, h1 = 2 * c + 1;
-  if (r == 0) {
-    if (h0 < G) { wm[h0] = m_run[0]; wm[8 + h0] = l_run[0]; }
-    if (h1 < G) { wm[h1] = m_run[1]; wm[8 + h1] = l_run[1]; }
+  if (c == 0 && r < G) {
+    wm[r] = m_run;
+    wm[8 + r] = l_run;
   }
 #pragma unroll
   for (int tt = 0; tt < KS; ++tt) {
@@ -825,6 +827,15 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
 // ===========================================================================
 // Kernels
 // ===========================================================================
+// Stages of a decode warp's ring inside the fused launch (which sizes its shared
+// memory for the chunk role).
+template <int FK, int FV, int D>
+struct FusedSmem {
+  static constexpr int kDec2 = DecodeSmem<FK, FV, D>::total(2);
+  static constexpr int kBytes = ChunkSmem<FK, FV, D>::kTotal > kDec2 ? ChunkSmem<FK, FV, D>::kTotal : kDec2;
+  static constexpr int kDecodeStages = DecodeSmem<FK, FV, D>::stages_for(kBytes - 16);
+};
+
 template <int FK, int FV, int D>
 __global__ void __launch_bounds__(kThreads, 1) mixed_attention_kernel(AttnParams p, unsigned int* err) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -832,28 +843,29 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_attention_kernel(AttnParams
   if (tile < p.n_chunk_tiles) {
     chunk_tile<FK, FV, D>(p, p.tiles[tile], smem, err);
   } else {
-    decode_tile<FK, FV, D>(p, p.tiles[tile], tile - p.n_chunk_tiles, smem, err);
+    decode_tile<FK, FV, D, FusedSmem<FK, FV, D>::kDecodeStages>(p, p.tiles[tile], tile - p.n_chunk_tiles, smem,
+                                                               err);
   }
 }
 
-template <int FK, int FV, int D>
-__global__ void __launch_bounds__(kThreads, 1) decode_attention_kernel(AttnParams p, unsigned int* err) {
+template <int FK, int FV, int D, int MINB, int NS>
+__global__ void __launch_bounds__(kThreads, MINB) decode_attention_kernel(AttnParams p, unsigned int* err) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tile = blockIdx.x + p.n_chunk_tiles;
-  decode_tile<FK, FV, D>(p, p.tiles[tile], blockIdx.x, smem, err);
+  decode_tile<FK, FV, D, NS>(p, p.tiles[tile], blockIdx.x, smem, err);
 }
 
 template <int FK, int FV, int D>
 cudaError_t launch_attention_t(const AttnParams& p, unsigned int* err, cudaStream_t s) {
+  using DS = DecodeSmem<FK, FV, D>;
   const int n_tiles = p.n_chunk_tiles + p.n_decode_tiles;
   if (n_tiles == 0) return cudaSuccess;
-  constexpr int kDec = DecodeSmem<FK, FV, D>::kTotal;
-  constexpr int kChunk = ChunkSmem<FK, FV, D>::kTotal;
-  constexpr int kFused = kDec > kChunk ? kDec : kChunk;
+  constexpr int kDec = DS::kTotal;
+  constexpr int kFused = FusedSmem<FK, FV, D>::kBytes;
+  auto* dec_kernel = decode_attention_kernel<FK, FV, D, DS::kSoloMinBlocks, DS::kSoloStages>;
   static bool configured = false;  // the attribute is per function, once per process
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_attention_kernel<FK, FV, D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kDec);
+    cudaError_t e = cudaFuncSetAttribute(dec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDec);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(mixed_attention_kernel<FK, FV, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kFused);
@@ -861,7 +873,7 @@ cudaError_t launch_attention_t(const AttnParams& p, unsigned int* err, cudaStrea
     configured = true;
   }
   if (p.n_chunk_tiles == 0) {
-    decode_attention_kernel<FK, FV, D><<<p.n_decode_tiles, kThreads, kDec, s>>>(p, err);
+    dec_kernel<<<p.n_decode_tiles, kThreads, kDec, s>>>(p, err);
   } else {
     mixed_attention_kernel<FK, FV, D><<<n_tiles, kThreads, kFused, s>>>(p, err);
   }
