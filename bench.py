@@ -177,6 +177,31 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------
+# Multi-process helpers (one process per GPU; replicas, no data-path collective)
+# --------------------------------------------------------------------------
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` over all ranks (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(tokens_per_step_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Tokens of all ranks per second: every rank runs its own batch each step."""
+    return world * tokens_per_step_per_rank / (ms_per_step / 1e3)
+
+
+def emit(line: dict, rank: int) -> None:
+    """Rank 0 prints the one JSON line; the other ranks print nothing."""
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
 # GPU arm
 # --------------------------------------------------------------------------
 def step_inputs(w: wl.Workload, pt: np.ndarray):
@@ -253,11 +278,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict:
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    total_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(t0.elapsed_time(t1), device=dev)
     app_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     attn_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     attn_mean = sum(attn_ms) / K
@@ -403,7 +424,7 @@ def main():
                 "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                  "sample": f"{len(sel)} of {w.total_q} query tokens per step"},
                 "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
+        emit(line, rank)
         return
 
     if world > 1:
@@ -424,7 +445,7 @@ def main():
     peaks = load_peaks()
     K = args.steps
     ms_step = res["total_ms"] / K
-    value = world * alg["tokens"] / (ms_step / 1e3)
+    value = whole_job_tokens_per_s(alg["tokens"], world, ms_step)
     attn_s = res["attn_ms"] / 1e3
     kv_gbs = alg["kv_bytes"] / attn_s / 1e9
     attn_gbs = alg["attn_bytes"] / attn_s / 1e9
@@ -457,7 +478,7 @@ def main():
         "append_gbs": alg["append_bytes"] / (res["append_ms"] / 1e3) / 1e9,
         "chunk_tflops": tflops,
         "roofline": roof,
-        "e2e": {"value": world * alg["tokens"] / (res["e2e_ms"] / 1e3), "unit": "tokens/s",
+        "e2e": {"value": whole_job_tokens_per_s(alg["tokens"], world, res["e2e_ms"]), "unit": "tokens/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
         "gpu_launches": 2 * K,
         "clocks": res["clocks"],
@@ -466,7 +487,7 @@ def main():
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.oracle_stride)
-    print(json.dumps(line))
+    emit(line, rank)
 
 
 if __name__ == "__main__":
