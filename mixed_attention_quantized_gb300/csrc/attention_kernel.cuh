@@ -20,12 +20,13 @@
 //
 // Chunk tiles (tensor-bound): a CTA owns 128 rows = 128/G query tokens x G
 // heads of one kv head.  K/V pages arrive raw through 1-D bulk copies (TMA
-// engine) into a stage whose refill overlaps the math of the previous tile.
-// They are dequantised into 128-byte-swizzled fp16 tiles -- an exact hi/lo
-// pair for quantised formats, since d*q needs up to 18 significant bits --
-// and S = Q K^T and O += P V run on tcgen05.mma (one MMA per half) with the
-// accumulators in TMEM.  The softmax threads own one TMEM lane (one query row)
-// each and write P as fp16 back into TMEM, where the PV MMA reads it.
+// engine) into two stages.  A dequant warp group turns them into
+// 128-byte-swizzled fp16 tiles -- an exact hi/lo pair for quantised formats,
+// since d*q needs up to 18 significant bits -- and issues S = Q K^T on
+// tcgen05.mma (Q and S in TMEM, one MMA per half); a softmax warp group, one
+// TMEM lane (query row) per thread, writes P as fp16 back into TMEM and issues
+// O += P V.  S is double-buffered so the next tile's QK and dequantisation
+// overlap this tile's softmax and PV.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -58,14 +59,13 @@ struct ChunkSmem {
   static constexpr int kRawVs = kRawVq + kPagesPerTile * kVqPage;
   static constexpr int kRawBytes = (kRawVs + kPagesPerTile * kVsPage + 1023) / 1024 * 1024;
   static constexpr int kTile = kChunkN * D * 2;             // one fp16 operand tile
-  static constexpr int kQ = 0;                              // [D/64][128 rows][128 B]
-  static constexpr int kKh = kQ + kChunkM * D * 2;          // [D/64][128 keys][128 B]
+  static constexpr int kKh = 0;                             // [D/64][128 keys][128 B]
   static constexpr int kKl = kKh + kTile;
   static constexpr int kVh = kKl + (kKLo ? kTile : 0);
   static constexpr int kVl = kVh + kTile;
-  static constexpr int kRaw = kVl + (kVLo ? kTile : 0);
-  static constexpr int kBar = kRaw + kRawBytes;
-  static constexpr int kTotal = kBar + 64 + 1024;           // + slack for 1024-B alignment
+  static constexpr int kRaw = kVl + (kVLo ? kTile : 0);     // two raw stages
+  static constexpr int kBar = kRaw + 2 * kRawBytes;         // 8 mbarriers, TMEM address, abort flag
+  static constexpr int kTotal = kBar + 128 + 1024;          // + slack for 1024-B alignment
   static_assert(kTotal <= 227 * 1024, "chunk tile does not fit in shared memory");
 };
 
@@ -526,18 +526,19 @@ __device__ __forceinline__ void split_hilo(uint32_t v, uint32_t s, uint32_t& hi,
   lo = hfma2_u32(v, s, hi ^ 0x80008000u);
 }
 
-// Dequantise one 128-key x D tile from the raw stage into swizzled fp16 tiles
-// (hi, and lo for quantised formats).  Keys at or past `valid_keys` (relative
-// to the tile) are written as zeros.
+// Dequantise one 128-key x D tile from a raw stage into swizzled fp16 tiles
+// (hi, and lo for quantised formats), by `nthr` threads numbered `t0`.
+// Keys at or past `valid_keys` (relative to the tile) are written as zeros.
 template <int F, int D, bool LO>
 __device__ __forceinline__ void dequant_tile(const uint8_t* raw_q, const uint8_t* raw_s, uint8_t* dst_hi,
-                                             uint8_t* dst_lo, int valid_keys) {
+                                             uint8_t* dst_lo, int valid_keys, int t0, int nthr) {
   constexpr int NB = D / kBlock;
   constexpr int CPR = D / 8;  // 16-byte fp16 chunks per key row
   constexpr int RB = F == MIXATTN_KV_F16 ? 2 * D : (F == MIXATTN_KV_Q8_0 ? D : D / 2);
   constexpr int PAGE_Q = kPage * RB;
   constexpr int PAGE_S = kPage * NB * 2;
-  for (int k = threadIdx.x; k < kChunkN * CPR; k += kThreads) {
+#pragma unroll 4
+  for (int k = t0; k < kChunkN * CPR; k += nthr) {
     const int key = k / CPR, dc = k - key * CPR;
     const int pj = key >> 5, kr = key & 31;
     uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = make_uint4(0u, 0u, 0u, 0u);
@@ -574,19 +575,34 @@ __device__ __forceinline__ void dequant_tile(const uint8_t* raw_q, const uint8_t
   }
 }
 
+// Chunk tile: 128 rows (128/G query tokens x G heads of kv head `t.kvh`) against
+// the keys they can see, in 128-key KV tiles j, by two groups of 4 warps:
+//   dequant group (warps 4-7): waits for raw tile j (bulk copies, two stages),
+//     dequantises K(j) once QK(j-1) has released the K tiles, issues QK(j) into
+//     S[j%2] (TMEM), dequantises V(j) once PV(j-1) has released the V tiles,
+//     signals vdeq_done, refills the raw stage with tile j+2;
+//   softmax group (warps 0-3, thread i = TMEM lane i = query row i): turns
+//     S[j%2] into P (fp16, written over the scores), waits for PV(j-1), rescales
+//     O when the row max moved, then issues PV(j).
+// TMEM: Q (A operand, fp16) | S0 | S1 | O (fp32).  Every wait is bounded; a
+// timeout in either group makes both leave their loops.
 template <int FK, int FV, int D>
 __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& t, uint8_t* smem_raw,
                                            unsigned int* err) {
   using L = ChunkSmem<FK, FV, D>;
   constexpr int NB = D / kBlock;
-  constexpr uint32_t kTmemCols = 256;  // S: 128 columns (P, fp16, overwrites its first 64); O: D columns
-  constexpr uint32_t kSCol = 0, kOCol = 128;
+  constexpr uint32_t kTmemCols = 512;
+  constexpr uint32_t kQCol = 0, kSCol0 = 128, kSCol1 = 256, kOCol = 384;
+  constexpr int kGroup = 128;  // threads per group
+  constexpr int kBarSoftmax = 1, kBarDequant = 2;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint64_t* s_done = full + 1;
-  uint64_t* o_done = full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 3);
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + L::kBar);  // [2]
+  uint64_t* qk_done = raw_full + 2;                                  // [2]
+  uint64_t* pv_done = raw_full + 4;                                  // [2]
+  uint64_t* vdeq_done = raw_full + 6;                                // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(raw_full + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(raw_full + 9);
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int G = p.group, lg = p.log2_group;
@@ -599,40 +615,54 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
   const int32_t* pt_row = p.page_table + (int64_t)t.row * p.max_pages;
 
   if (tid == 0) {
-    mbar_init(full, 1);
-    mbar_init(s_done, 1);
-    mbar_init(o_done, 1);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mbar_init(raw_full + i, 1);
+    *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-
-  // ---- Q tile: row i = token (i >> lg), head (i & (G-1)) -> swizzled fp16 ----
-  {
-    constexpr int CPR = D / 8;
-    for (int k = tid; k < kChunkM * CPR; k += kThreads) {
-      const int row = k / CPR, dc = k - row * CPR;
-      const int tok = row >> lg, h = row & (G - 1);
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (tok < t.count) {
-        const uint16_t* src = static_cast<const uint16_t*>(p.q) +
-                              ((int64_t)(ri.q_start + t.begin + tok) * p.hq + (int64_t)g * G + h) * D + 8 * dc;
-        v = ldg_u128(src);
-      }
-      *reinterpret_cast<uint4*>(smem + L::kQ + (dc >> 3) * (kChunkM * 128) + sw128_off(row, dc & 7)) = v;
-    }
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // ---- producer: raw pages of KV tile jj into the stage ----
-  auto issue_raw = [&](int jj) {
-    uint8_t* raw = smem + L::kRaw;
+  // softmax state: thread i < 128 owns row i (TMEM lane i)
+  const int row = tid & 127;
+  const int tok = row >> lg;
+  const bool row_valid = tid < 128 && tok < t.count;
+  const int pos = ri.q_offset + t.begin + min(tok, t.count - 1);
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+
+  // ---- Q row -> TMEM (the A operand of QK), two fp16 per column ----
+  if (tid < kGroup) {
+    const uint16_t* src = static_cast<const uint16_t*>(p.q) +
+                          ((int64_t)(ri.q_start + t.begin + min(tok, t.count - 1)) * p.hq + (int64_t)g * G +
+                           (row & (G - 1))) * D;
+#pragma unroll
+    for (int ch = 0; ch < D / 64; ++ch) {
+      uint32_t v[32];
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        const uint4 w = tok < t.count ? ldg_u128(src + 64 * ch + 8 * q4) : make_uint4(0u, 0u, 0u, 0u);
+        v[4 * q4] = w.x;
+        v[4 * q4 + 1] = w.y;
+        v[4 * q4 + 2] = w.z;
+        v[4 * q4 + 3] = w.w;
+      }
+      tmem_st32(tmem + lane_base + kQCol + 32 * ch, v);
+    }
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // ---- producer: raw pages of KV tile jj into stage st ----
+  auto issue_raw = [&](int jj, int st) {
+    uint8_t* raw = smem + L::kRaw + st * L::kRawBytes;
     uint32_t bytes = 0;
     int pids[L::kPagesPerTile];
 #pragma unroll
@@ -649,152 +679,210 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
       pids[pj] = pid;
       if (pid >= 0) bytes += L::kKqPage + L::kKsPage + L::kVqPage + L::kVsPage;
     }
-    mbar_arrive_expect_tx(full, bytes);
+    mbar_arrive_expect_tx(&raw_full[st], bytes);
 #pragma unroll
     for (int pj = 0; pj < L::kPagesPerTile; ++pj) {
       const int pid = pids[pj];
       if (pid < 0) continue;
       const int64_t prow = ((int64_t)pid * p.hkv + g) * kPage;  // first plane row of (page, head)
-      bulk_g2s(raw + L::kRawKq + pj * L::kKqPage, p.k_quant + prow * (L::kKqPage / kPage), L::kKqPage, full);
-      if (L::kKsPage) bulk_g2s(raw + L::kRawKs + pj * L::kKsPage, p.k_scale + prow * NB, L::kKsPage, full);
-      bulk_g2s(raw + L::kRawVq + pj * L::kVqPage, p.v_quant + prow * (L::kVqPage / kPage), L::kVqPage, full);
-      if (L::kVsPage) bulk_g2s(raw + L::kRawVs + pj * L::kVsPage, p.v_scale + prow * NB, L::kVsPage, full);
+      bulk_g2s(raw + L::kRawKq + pj * L::kKqPage, p.k_quant + prow * (L::kKqPage / kPage), L::kKqPage,
+               &raw_full[st]);
+      if (L::kKsPage)
+        bulk_g2s(raw + L::kRawKs + pj * L::kKsPage, p.k_scale + prow * NB, L::kKsPage, &raw_full[st]);
+      bulk_g2s(raw + L::kRawVq + pj * L::kVqPage, p.v_quant + prow * (L::kVqPage / kPage), L::kVqPage,
+               &raw_full[st]);
+      if (L::kVsPage)
+        bulk_g2s(raw + L::kRawVs + pj * L::kVsPage, p.v_scale + prow * NB, L::kVsPage, &raw_full[st]);
     }
   };
 
-  const int issuer = 128;  // warp 4, lane 0: copies and MMAs
-  int raw_issued = 0, raw_consumed = 0;
-  if (tid == issuer) {
-    issue_raw(0);
-    raw_issued = 1;
-  }
-
-  // softmax state: thread i < 128 owns row i (TMEM lane i)
-  const int row = tid & 127;
-  const int tok = row >> lg;
-  const bool row_valid = tid < 128 && tok < t.count;
-  const int pos = ri.q_offset + t.begin + min(tok, t.count - 1);
-  float m_run = -CUDART_INF_F, l_run = 0.f;
-  const float sl2 = p.scale_log2;
-  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  bool ok = true;
-  int pv_issued = 0;
-
   constexpr uint32_t kIdescQK = idesc_f16_f32(128, kChunkN, false, false);
   constexpr uint32_t kIdescPV = idesc_f16_f32(128, D, false, true);
-  const uint32_t sQ = smem_u32(smem + L::kQ);
   const uint32_t sKh = smem_u32(smem + L::kKh), sKl = smem_u32(smem + L::kKl);
   const uint32_t sVh = smem_u32(smem + L::kVh), sVl = smem_u32(smem + L::kVl);
+  bool ok = true;
+  int qk_issued = 0, pv_issued = 0, raw_issued = 0;
+  float m_run = -CUDART_INF_F, l_run = 0.f;
 
-  for (int j = 0; j < n_kv; ++j) {
-    ok = mbar_wait(full, (uint32_t)(j & 1), err) && ok;
-    raw_consumed = j + 1;
-    if (j > 0) ok = mbar_wait(o_done, (uint32_t)((j - 1) & 1), err) && ok;
-    tc_fence_after();
-    const uint8_t* raw = smem + L::kRaw;
-    const int valid_keys = key_end - j * kChunkN;
-    dequant_tile<FK, D, L::kKLo>(raw + L::kRawKq, raw + L::kRawKs, smem + L::kKh, smem + L::kKl, valid_keys);
-    dequant_tile<FV, D, L::kVLo>(raw + L::kRawVq, raw + L::kRawVs, smem + L::kVh, smem + L::kVl, valid_keys);
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == issuer) {
-      if (j + 1 < n_kv) {  // the stage is free again: the copy overlaps this tile's math
-        issue_raw(j + 1);
-        raw_issued = j + 2;
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t off = (uint32_t)((ks >> 2) * (128 * 128) + (ks & 3) * 32);
-        const uint64_t qd = sw128_desc(sQ + off, 16, 1024);
-        tc_mma_ss(tmem + kSCol, qd, sw128_desc(sKh + off, 16, 1024), kIdescQK, ks > 0 ? 1u : 0u);
-        if (L::kKLo) tc_mma_ss(tmem + kSCol, qd, sw128_desc(sKl + off, 16, 1024), kIdescQK, 1u);
-      }
-      tc_commit(s_done);
+  if (tid >= kGroup) {
+    // ======================= dequant group =======================
+    const int dt = tid - kGroup;
+    if (dt == 0) {
+      for (int jj = 0; jj < 2 && jj < n_kv; ++jj) issue_raw(jj, jj);
+      raw_issued = min(2, n_kv);
     }
-    if (tid < 128) {
-      ok = mbar_wait(s_done, (uint32_t)(j & 1), err) && ok;
+    for (int j = 0; j < n_kv; ++j) {
+      const int st = j & 1;
+      const uint32_t ph = (uint32_t)((j >> 1) & 1), ph_prev = (uint32_t)(((j - 1) >> 1) & 1);
+      ok = mbar_wait(&raw_full[st], ph, err) && ok;
+      if (j > 0) ok = mbar_wait(&qk_done[(j - 1) & 1], ph_prev, err) && ok;  // K tiles free
       tc_fence_after();
-      const int kbase = j * kChunkN;
-      // pass 1: row max of the scaled, masked scores
-      float mx = -CUDART_INF_F;
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kSCol + 32 * ch, v);
-        tmem_wait_ld();
+      const uint8_t* raw = smem + L::kRaw + st * L::kRawBytes;
+      const int valid_keys = key_end - j * kChunkN;
+      dequant_tile<FK, D, L::kKLo>(raw + L::kRawKq, raw + L::kRawKs, smem + L::kKh, smem + L::kKl, valid_keys, dt,
+                                   kGroup);
+      fence_proxy_async_smem();
+      if (bar_any(kBarDequant, kGroup, !ok || *abort_flag)) {  // one decision for the group
+        *abort_flag = 1;
+        break;
+      }
+      if (dt == 0) {
+        tc_fence_after();
+        const uint32_t s_col = st ? kSCol1 : kSCol0;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int key = kbase + 32 * ch + e;
-          const float x = key <= pos ? __uint_as_float(v[e]) * sl2 : -CUDART_INF_F;
-          mx = fmaxf(mx, x);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (uint32_t)((ks >> 2) * (kChunkN * 128) + (ks & 3) * 32);
+          tc_mma_ts(tmem + s_col, tmem + kQCol + 8 * ks, sw128_desc(sKh + off, 16, 1024), kIdescQK,
+                    ks > 0 ? 1u : 0u);
+          if (L::kKLo) tc_mma_ts(tmem + s_col, tmem + kQCol + 8 * ks, sw128_desc(sKl + off, 16, 1024), kIdescQK, 1u);
+        }
+        tc_commit(&qk_done[st]);
+        ++qk_issued;
+      }
+      if (j > 0) ok = mbar_wait(&pv_done[(j - 1) & 1], ph_prev, err) && ok;  // V tiles free
+      tc_fence_after();
+      dequant_tile<FV, D, L::kVLo>(raw + L::kRawVq, raw + L::kRawVs, smem + L::kVh, smem + L::kVl, valid_keys, dt,
+                                   kGroup);
+      fence_proxy_async_smem();
+      if (bar_any(kBarDequant, kGroup, !ok || *abort_flag)) {  // one decision for the group
+        *abort_flag = 1;
+        break;
+      }
+      if (dt == 0) {
+        mbar_arrive(&vdeq_done[st]);
+        if (j + 2 < n_kv) {  // the stage is consumed: refill it with tile j+2
+          issue_raw(j + 2, st);
+          raw_issued = j + 3;
         }
       }
-      const float m_new = fmaxf(m_run, mx);
+    }
+    if (dt == 0) {
+      // nothing this group started may still run when TMEM and the stages are released
+      if (qk_issued > 0) mbar_wait(&qk_done[(qk_issued - 1) & 1], (uint32_t)(((qk_issued - 1) >> 1) & 1), err);
+      for (int jj = max(0, raw_issued - 2); jj < raw_issued; ++jj)
+        mbar_wait(&raw_full[jj & 1], (uint32_t)((jj >> 1) & 1), err);
+    }
+  } else {
+    // ======================= softmax group =======================
+    const float sl2 = p.scale_log2;
+    for (int j = 0; j < n_kv; ++j) {
+      const int st = j & 1;
+      const uint32_t ph = (uint32_t)((j >> 1) & 1), ph_prev = (uint32_t)(((j - 1) >> 1) & 1);
+      const uint32_t s_col = st ? kSCol1 : kSCol0;
+      ok = mbar_wait(&qk_done[st], ph, err) && ok;
+      tc_fence_after();
+      const int kbase = j * kChunkN;
+      // the tile's 128 scores of this row, held in registers (one TMEM read)
+      uint32_t v0[32], v1[32], v2[32], v3[32];
+      tmem_ld32(tmem + lane_base + s_col + 0, v0);
+      tmem_ld32(tmem + lane_base + s_col + 32, v1);
+      tmem_ld32(tmem + lane_base + s_col + 64, v2);
+      tmem_ld32(tmem + lane_base + s_col + 96, v3);
+      tmem_wait_ld();
+      // causal mask: only a warp whose tile crosses the diagonal pays for it
+      if (__any_sync(0xFFFFFFFFu, kbase + kChunkN - 1 > pos)) {
+        const uint32_t ninf = __float_as_uint(-CUDART_INF_F);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          if (kbase + e > pos) v0[e] = ninf;
+          if (kbase + 32 + e > pos) v1[e] = ninf;
+          if (kbase + 64 + e > pos) v2[e] = ninf;
+          if (kbase + 96 + e > pos) v3[e] = ninf;
+        }
+      }
+      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        mx0 = fmaxf(mx0, __uint_as_float(v0[e]));
+        mx1 = fmaxf(mx1, __uint_as_float(v1[e]));
+        mx2 = fmaxf(mx2, __uint_as_float(v2[e]));
+        mx3 = fmaxf(mx3, __uint_as_float(v3[e]));
+      }
+      // running max in log2 units (the score scale is positive, so it commutes with max)
+      const float m_new = fmaxf(m_run, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
       const float alpha = ex2(m_run - m_new);
-      // pass 2: P = 2^(s - m) as fp16 into TMEM over the consumed scores, row sums
-      float sum = 0.f;
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kSCol + 32 * ch, v);
-        tmem_wait_ld();
+      const float neg_m = -m_new;
+      // P = 2^(s*scale - m) as fp16 into TMEM over the consumed scores; row sums
+      float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+      {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const int key = kbase + 32 * ch + e;
-          const float x0 = key <= pos ? __uint_as_float(v[e]) * sl2 : -CUDART_INF_F;
-          const float x1 = key + 1 <= pos ? __uint_as_float(v[e + 1]) * sl2 : -CUDART_INF_F;
-          const float p0 = ex2(x0 - m_new), p1 = ex2(x1 - m_new);
-          sum += p0 + p1;
-          pk[e >> 1] = pack_f16x2(p0, p1);
+          const float a0 = ex2(fmaf(__uint_as_float(v0[e]), sl2, neg_m));
+          const float a1 = ex2(fmaf(__uint_as_float(v0[e + 1]), sl2, neg_m));
+          sum0 += a0 + a1;
+          pk[e >> 1] = pack_f16x2(a0, a1);
         }
-        tmem_st16(tmem + lane_base + kSCol + 16 * ch, pk);
+        tmem_st16(tmem + lane_base + s_col + 0, pk);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float a0 = ex2(fmaf(__uint_as_float(v1[e]), sl2, neg_m));
+          const float a1 = ex2(fmaf(__uint_as_float(v1[e + 1]), sl2, neg_m));
+          sum1 += a0 + a1;
+          pk[e >> 1] = pack_f16x2(a0, a1);
+        }
+        tmem_st16(tmem + lane_base + s_col + 16, pk);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float a0 = ex2(fmaf(__uint_as_float(v2[e]), sl2, neg_m));
+          const float a1 = ex2(fmaf(__uint_as_float(v2[e + 1]), sl2, neg_m));
+          sum2 += a0 + a1;
+          pk[e >> 1] = pack_f16x2(a0, a1);
+        }
+        tmem_st16(tmem + lane_base + s_col + 32, pk);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float a0 = ex2(fmaf(__uint_as_float(v3[e]), sl2, neg_m));
+          const float a1 = ex2(fmaf(__uint_as_float(v3[e + 1]), sl2, neg_m));
+          sum3 += a0 + a1;
+          pk[e >> 1] = pack_f16x2(a0, a1);
+        }
+        tmem_st16(tmem + lane_base + s_col + 48, pk);
       }
+      const float sum = (sum0 + sum1) + (sum2 + sum3);
       l_run = l_run * alpha + sum;
       m_run = m_new;
-      // rescale the running O (TMEM) when this row's max moved
-      if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+      // the running O may be rescaled only once PV(j-1) has finished with it
+      if (j > 0) {
+        ok = mbar_wait(&pv_done[(j - 1) & 1], ph_prev, err) && ok;
+        tc_fence_after();
+        if (__any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
 #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + kOCol + 32 * ch, v);
-          tmem_wait_ld();
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + kOCol + 32 * ch, v);
+            tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tmem_st32(tmem + lane_base + kOCol + 32 * ch, v);
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st32(tmem + lane_base + kOCol + 32 * ch, v);
+          }
         }
       }
       tmem_wait_st();
-    }
-    tc_fence_before();
-    if (!__syncthreads_and(ok)) {  // a bounded wait gave up somewhere: leave together
-      ok = false;
-      break;
-    }
-    if (tid == issuer) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < kChunkN / 16; ++kk) {
-        const uint32_t pa = tmem + kSCol + 8 * kk;  // P columns of keys 16kk..16kk+15
-        const uint32_t boff = (uint32_t)(kk * 16 * 128);
-        const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-        tc_mma_ts(tmem + kOCol, pa, sw128_desc(sVh + boff, kChunkN * 128, 1024), kIdescPV, acc);
-        if (L::kVLo) tc_mma_ts(tmem + kOCol, pa, sw128_desc(sVl + boff, kChunkN * 128, 1024), kIdescPV, 1u);
+      tc_fence_before();
+      if (bar_any(kBarSoftmax, kGroup, !ok || *abort_flag)) {  // one decision for the group
+        *abort_flag = 1;
+        break;
       }
-      tc_commit(o_done);
-      ++pv_issued;
+      if (tid == 0) {
+        ok = mbar_wait(&vdeq_done[st], ph, err) && ok;  // V(j) tiles written
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kChunkN / 16; ++kk) {
+          const uint32_t pa = tmem + s_col + 8 * kk;  // P columns of keys 16kk..16kk+15
+          const uint32_t boff = (uint32_t)(kk * 16 * 128);
+          const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+          tc_mma_ts(tmem + kOCol, pa, sw128_desc(sVh + boff, kChunkN * 128, 1024), kIdescPV, acc);
+          if (L::kVLo) tc_mma_ts(tmem + kOCol, pa, sw128_desc(sVl + boff, kChunkN * 128, 1024), kIdescPV, 1u);
+        }
+        tc_commit(&pv_done[st]);
+        ++pv_issued;
+      }
     }
-  }
-
-  // ---- epilogue: O / l -> fp16 ----
-  if (tid == issuer) {
-    // nothing the issuer started may still be running when TMEM and the stage are released
-    if (pv_issued > 0) mbar_wait(o_done, (uint32_t)((pv_issued - 1) & 1), err);
-    if (raw_issued > raw_consumed) mbar_wait(full, (uint32_t)((raw_issued - 1) & 1), err);
-  }
-  if (tid < 128 && ok) ok = mbar_wait(o_done, (uint32_t)((n_kv - 1) & 1), err);
-  if (tid < 128) {
+    // ---- epilogue: O / l -> fp16 ----
+    const bool done = !*abort_flag;
+    if (tid == 0 && pv_issued > 0) mbar_wait(&pv_done[(pv_issued - 1) & 1], (uint32_t)(((pv_issued - 1) >> 1) & 1), err);
+    if (done) ok = mbar_wait(&pv_done[(n_kv - 1) & 1], (uint32_t)(((n_kv - 1) >> 1) & 1), err) && ok;
     tc_fence_after();
     const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
     uint16_t* dst = static_cast<uint16_t*>(p.o) +
@@ -808,7 +896,7 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
 #pragma unroll
       for (int e = 0; e < 32; e += 2)
         pk[e >> 1] = pack_f16x2(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
-      if (row_valid && ok) {
+      if (row_valid && ok && done) {
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
           *reinterpret_cast<uint4*>(dst + 32 * ch + 8 * q4) =
@@ -824,9 +912,6 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
   }
 }
 
-// ===========================================================================
-// Kernels
-// ===========================================================================
 // Stages of a decode warp's ring inside the fused launch (which sizes its shared
 // memory for the chunk role).
 template <int FK, int FV, int D>
