@@ -527,51 +527,78 @@ __device__ __forceinline__ void split_hilo(uint32_t v, uint32_t s, uint32_t& hi,
 }
 
 // Dequantise one 128-key x D tile from a raw stage into swizzled fp16 tiles
-// (hi, and lo for quantised formats), by `nthr` threads numbered `t0`.
+// (hi, and lo for quantised formats), by the 128 threads numbered t0 = 0..127.
 // Keys at or past `valid_keys` (relative to the tile) are written as zeros.
+//
+// Thread t0 owns one 16-byte output column chunk (dc = t0 % (D/8)) and the keys
+// t0 / (D/8) + i * KPI.  The raw stage holds the tile's 4 pages back to back,
+// so the source row of a key is raw + key * row_bytes; KPI is a multiple of 8,
+// so the swizzle term (key & 7) is fixed per thread and every address is a
+// base plus i times a constant.  Loads for four keys are issued before any
+// conversion.
 template <int F, int D, bool LO>
-__device__ __forceinline__ void dequant_tile(const uint8_t* raw_q, const uint8_t* raw_s, uint8_t* dst_hi,
-                                             uint8_t* dst_lo, int valid_keys, int t0, int nthr) {
+__device__ __forceinline__ void dequant_tile(const uint8_t* __restrict__ raw_q, const uint8_t* __restrict__ raw_s,
+                                             uint8_t* __restrict__ dst_hi, uint8_t* __restrict__ dst_lo,
+                                             int valid_keys, int t0) {
   constexpr int NB = D / kBlock;
-  constexpr int CPR = D / 8;  // 16-byte fp16 chunks per key row
+  constexpr int CPR = D / 8;           // 16-byte fp16 chunks per key row
+  constexpr int KPI = 128 / CPR;       // keys advanced per step (8 or 16)
+  constexpr int ITER = kChunkN / KPI;  // steps per thread (16 or 8)
   constexpr int RB = F == MIXATTN_KV_F16 ? 2 * D : (F == MIXATTN_KV_Q8_0 ? D : D / 2);
-  constexpr int PAGE_Q = kPage * RB;
-  constexpr int PAGE_S = kPage * NB * 2;
-#pragma unroll 4
-  for (int k = t0; k < kChunkN * CPR; k += nthr) {
-    const int key = k / CPR, dc = k - key * CPR;
-    const int pj = key >> 5, kr = key & 31;
-    uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = make_uint4(0u, 0u, 0u, 0u);
-    if (key < valid_keys) {
-      const uint8_t* qrow = raw_q + pj * PAGE_Q + kr * RB;
+  static_assert(KPI % 8 == 0, "the swizzle phase must be fixed per thread");
+  const int dc = t0 % CPR, key0 = t0 / CPR;
+  const int b = dc >> 2, half = dc >> 3, cc = dc & 7;
+  int src_col;
+  if (F == MIXATTN_KV_F16) src_col = 16 * dc;
+  else if (F == MIXATTN_KV_Q8_0) src_col = 8 * dc;
+  else src_col = 16 * b + 8 * (dc & 1);
+  const int shift = F == MIXATTN_KV_Q4_0 ? ((dc >> 1) & 1) * 4 : 0;  // low nibbles, then high nibbles
+  const uint8_t* src = raw_q + key0 * RB + src_col;
+  const uint8_t* ssrc = raw_s + key0 * NB * 2 + 2 * b;
+  const uint32_t doff = (uint32_t)(half * (kChunkN * 128) + key0 * 128 + ((cc ^ (key0 & 7)) << 4));
+  const bool all_valid = valid_keys >= kChunkN;
+#pragma unroll
+  for (int i0 = 0; i0 < ITER; i0 += 4) {
+    uint4 w[4];
+    uint32_t s2[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u;
       if (F == MIXATTN_KV_F16) {
-        hi = *reinterpret_cast<const uint4*>(qrow + 16 * dc);
+        w[u] = *reinterpret_cast<const uint4*>(src + i * KPI * RB);
       } else {
-        const int b = dc >> 2;
-        const uint16_t sh = *reinterpret_cast<const uint16_t*>(raw_s + pj * PAGE_S + (kr * NB + b) * 2);
-        const uint32_t s2 = (uint32_t)sh | ((uint32_t)sh << 16);
-        uint32_t h0, h1, h2, h3;
-        if (F == MIXATTN_KV_Q8_0) {
-          const uint2 w = *reinterpret_cast<const uint2*>(qrow + 8 * dc);
-          s8x4_to_f16x2x2(w.x, h0, h1);
-          s8x4_to_f16x2x2(w.y, h2, h3);
-        } else {
-          const int e = dc & 3;  // 8-element group of the block: 0,1 low nibbles; 2,3 high nibbles
-          const uint2 w = *reinterpret_cast<const uint2*>(qrow + 16 * b + 8 * (e & 1));
-          const int shift = (e >> 1) * 4;
-          u4x4_to_f16x2x2((w.x >> shift) & 0x0F0F0F0Fu, h0, h1);
-          u4x4_to_f16x2x2((w.y >> shift) & 0x0F0F0F0Fu, h2, h3);
-        }
-        split_hilo(h0, s2, hi.x, lo.x);
-        split_hilo(h1, s2, hi.y, lo.y);
-        split_hilo(h2, s2, hi.z, lo.z);
-        split_hilo(h3, s2, hi.w, lo.w);
+        const uint2 x = *reinterpret_cast<const uint2*>(src + i * KPI * RB);
+        w[u] = make_uint4(x.x, x.y, 0u, 0u);
+        const uint32_t sh = *reinterpret_cast<const uint16_t*>(ssrc + i * KPI * NB * 2);
+        s2[u] = sh | (sh << 16);
       }
     }
-    const int half = dc >> 3, cc = dc & 7;
-    const uint32_t off = half * (kChunkN * 128) + sw128_off(key, cc);
-    *reinterpret_cast<uint4*>(dst_hi + off) = hi;
-    if (LO) *reinterpret_cast<uint4*>(dst_lo + off) = lo;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u;
+      const bool valid = all_valid || key0 + i * KPI < valid_keys;
+      uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = make_uint4(0u, 0u, 0u, 0u);
+      if (valid) {
+        if (F == MIXATTN_KV_F16) {
+          hi = w[u];
+        } else {
+          uint32_t h0, h1, h2, h3;
+          if (F == MIXATTN_KV_Q8_0) {
+            s8x4_to_f16x2x2(w[u].x, h0, h1);
+            s8x4_to_f16x2x2(w[u].y, h2, h3);
+          } else {
+            u4x4_to_f16x2x2((w[u].x >> shift) & 0x0F0F0F0Fu, h0, h1);
+            u4x4_to_f16x2x2((w[u].y >> shift) & 0x0F0F0F0Fu, h2, h3);
+          }
+          split_hilo(h0, s2[u], hi.x, lo.x);
+          split_hilo(h1, s2[u], hi.y, lo.y);
+          split_hilo(h2, s2[u], hi.z, lo.z);
+          split_hilo(h3, s2[u], hi.w, lo.w);
+        }
+      }
+      *reinterpret_cast<uint4*>(dst_hi + doff + i * KPI * 128) = hi;
+      if (LO) *reinterpret_cast<uint4*>(dst_lo + doff + i * KPI * 128) = lo;
+    }
   }
 }
 
@@ -719,8 +746,7 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
       tc_fence_after();
       const uint8_t* raw = smem + L::kRaw + st * L::kRawBytes;
       const int valid_keys = key_end - j * kChunkN;
-      dequant_tile<FK, D, L::kKLo>(raw + L::kRawKq, raw + L::kRawKs, smem + L::kKh, smem + L::kKl, valid_keys, dt,
-                                   kGroup);
+      dequant_tile<FK, D, L::kKLo>(raw + L::kRawKq, raw + L::kRawKs, smem + L::kKh, smem + L::kKl, valid_keys, dt);
       fence_proxy_async_smem();
       if (bar_any(kBarDequant, kGroup, !ok || *abort_flag)) {  // one decision for the group
         *abort_flag = 1;
@@ -741,8 +767,7 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
       }
       if (j > 0) ok = mbar_wait(&pv_done[(j - 1) & 1], ph_prev, err) && ok;  // V tiles free
       tc_fence_after();
-      dequant_tile<FV, D, L::kVLo>(raw + L::kRawVq, raw + L::kRawVs, smem + L::kVh, smem + L::kVl, valid_keys, dt,
-                                   kGroup);
+      dequant_tile<FV, D, L::kVLo>(raw + L::kRawVq, raw + L::kRawVs, smem + L::kVh, smem + L::kVl, valid_keys, dt);
       fence_proxy_async_smem();
       if (bar_any(kBarDequant, kGroup, !ok || *abort_flag)) {  // one decision for the group
         *abort_flag = 1;
