@@ -52,20 +52,25 @@ struct ChunkSmem {
   // quantised formats carry an exact low half: d*q = hi + lo, both fp16
   static constexpr bool kKLo = FK != MIXATTN_KV_F16;
   static constexpr bool kVLo = FV != MIXATTN_KV_F16;
-  // raw stage: [Kq x4][Ks x4][Vq x4][Vs x4]
-  static constexpr int kRawKq = 0;
-  static constexpr int kRawKs = kRawKq + kPagesPerTile * kKqPage;
-  static constexpr int kRawVq = kRawKs + kPagesPerTile * kKsPage;
-  static constexpr int kRawVs = kRawVq + kPagesPerTile * kVqPage;
-  static constexpr int kRawBytes = (kRawVs + kPagesPerTile * kVsPage + 1023) / 1024 * 1024;
   static constexpr int kTile = kChunkN * D * 2;             // one fp16 operand tile
   static constexpr int kKh = 0;                             // [D/64][128 keys][128 B]
   static constexpr int kKl = kKh + kTile;
   static constexpr int kVh = kKl + (kKLo ? kTile : 0);
   static constexpr int kVl = kVh + kTile;
-  static constexpr int kRaw = kVl + (kVLo ? kTile : 0);     // two raw stages
-  static constexpr int kBar = kRaw + 2 * kRawBytes;         // 8 mbarriers, TMEM address, abort flag
-  static constexpr int kTotal = kBar + 128 + 1024;          // + slack for 1024-B alignment
+  // raw K stage: [Kq x4][Ks x4]; raw V stage: [Vq x4][Vs x4]
+  static constexpr int kKsOff = kPagesPerTile * kKqPage;
+  static constexpr int kVsOff = kPagesPerTile * kVqPage;
+  static constexpr int kKRawBytes = (kKsOff + kPagesPerTile * kKsPage + 1023) / 1024 * 1024;
+  static constexpr int kVRawBytes = (kVsOff + kPagesPerTile * kVsPage + 1023) / 1024 * 1024;
+  static constexpr int kBarBytes = 256;                     // mbarriers, TMEM address, abort flag
+  static constexpr int kRawBudget = 227 * 1024 - 1024 - kBarBytes - (kVl + (kVLo ? kTile : 0));
+  // three raw K stages where they fit (K is dequantised first), then three raw V stages
+  static constexpr int kKStages = 3 * kKRawBytes + 2 * kVRawBytes <= kRawBudget ? 3 : 2;
+  static constexpr int kVStages = kKStages * kKRawBytes + 3 * kVRawBytes <= kRawBudget ? 3 : 2;
+  static constexpr int kKRaw = kVl + (kVLo ? kTile : 0);
+  static constexpr int kVRaw = kKRaw + kKStages * kKRawBytes;
+  static constexpr int kBar = kVRaw + kVStages * kVRawBytes;
+  static constexpr int kTotal = kBar + kBarBytes + 1024;   // + slack for 1024-B alignment
   static_assert(kTotal <= 227 * 1024, "chunk tile does not fit in shared memory");
 };
 
@@ -143,6 +148,10 @@ __device__ __forceinline__ void load_scales(const uint8_t* p, float (&out)[NB]) 
     out[NB - 1] = __half2float(__ushort_as_half(a >> 16));
   }
 }
+
+// Barrier over the 8 warps of a decode tile (a fused-launch CTA has more warps,
+// which leave before the tile starts).
+__device__ __forceinline__ void decode_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
 
 template <int FK, int FV, int D, int NS>
 __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc& t, int dec_idx, uint8_t* smem,
@@ -423,7 +432,7 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   // ---------------- warp partial -> shared memory ----------------
   l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 1);
   l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 2);
-  __syncthreads();  // the staging rings are no longer needed: reuse them as merge scratch
+  decode_sync();  // the staging rings are no longer needed: reuse them as merge scratch
   float* ws = reinterpret_cast<float*>(smem);
   float* wm = ws + warp * S::kPerWarp;  // m[8], l[8], O[8][D]
   const int h0 = 2 * c, h1 = 2 * c + 1;
@@ -443,7 +452,7 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
       wm[16 + h1 * D + d_hi] = o_acc[tt][3];
     }
   }
-  __syncthreads();
+  decode_sync();
 
   // ---------------- merge the 8 warps ----------------
   const int n_out = G * D;
@@ -476,13 +485,13 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
 
   // ---------------- last CTA of (row, kv head) merges the splits ----------------
   __threadfence();
-  __syncthreads();
+  decode_sync();
   __shared__ int s_last;
   if (tid == 0) {
     const unsigned prev = atomicAdd(&p.counters[(int64_t)t.row * p.hkv + g], 1u);
     s_last = (prev == (unsigned)(ri.n_splits - 1));
   }
-  __syncthreads();
+  decode_sync();
   if (!s_last) return;
   __threadfence();
   const int first = dec_idx - split;
@@ -523,11 +532,12 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int cc) {
 // the scale's ulp (>= 2^-24) below 2^8 of them.  So hi + lo == v*s exactly.
 __device__ __forceinline__ void split_hilo(uint32_t v, uint32_t s, uint32_t& hi, uint32_t& lo) {
   hi = hmul2_u32(v, s);
-  lo = hfma2_u32(v, s, hi ^ 0x80008000u);
+  lo = hfma2_u32(v, s, hneg2_u32(hi));  // the negation folds into the fma
 }
 
-// Dequantise one 128-key x D tile from a raw stage into swizzled fp16 tiles
-// (hi, and lo for quantised formats), by the 128 threads numbered t0 = 0..127.
+// Dequantise key half H (keys 64H..64H+63) of one 128-key x D tile from a raw
+// stage into swizzled fp16 tiles (hi, and lo for quantised formats), by the 128
+// threads numbered t0 = 0..127.
 // Keys at or past `valid_keys` (relative to the tile) are written as zeros.
 //
 // Thread t0 owns one 16-byte output column chunk (dc = t0 % (D/8)) and the keys
@@ -537,9 +547,9 @@ __device__ __forceinline__ void split_hilo(uint32_t v, uint32_t s, uint32_t& hi,
 // base plus i times a constant.  Loads for four keys are issued before any
 // conversion.
 template <int F, int D, bool LO>
-__device__ __forceinline__ void dequant_tile(const uint8_t* __restrict__ raw_q, const uint8_t* __restrict__ raw_s,
+__device__ __forceinline__ void dequant_half_body(const uint8_t* __restrict__ raw_q, const uint8_t* __restrict__ raw_s,
                                              uint8_t* __restrict__ dst_hi, uint8_t* __restrict__ dst_lo,
-                                             int valid_keys, int t0) {
+                                                  int valid_keys, int t0, int H) {
   constexpr int NB = D / kBlock;
   constexpr int CPR = D / 8;           // 16-byte fp16 chunks per key row
   constexpr int KPI = 128 / CPR;       // keys advanced per step (8 or 16)
@@ -553,12 +563,15 @@ __device__ __forceinline__ void dequant_tile(const uint8_t* __restrict__ raw_q, 
   else if (F == MIXATTN_KV_Q8_0) src_col = 8 * dc;
   else src_col = 16 * b + 8 * (dc & 1);
   const int shift = F == MIXATTN_KV_Q4_0 ? ((dc >> 1) & 1) * 4 : 0;  // low nibbles, then high nibbles
-  const uint8_t* src = raw_q + key0 * RB + src_col;
-  const uint8_t* ssrc = raw_s + key0 * NB * 2 + 2 * b;
-  const uint32_t doff = (uint32_t)(half * (kChunkN * 128) + key0 * 128 + ((cc ^ (key0 & 7)) << 4));
-  const bool all_valid = valid_keys >= kChunkN;
+  const int kh = key0 + kChunkN / 2 * H;  // first key of this thread in the half
+  const uint8_t* src = raw_q + kh * RB + src_col;
+  const uint8_t* ssrc = raw_s + kh * NB * 2 + 2 * b;
+  const uint32_t doff = (uint32_t)(half * (kChunkN * 128) + kh * 128 + ((cc ^ (key0 & 7)) << 4));
+  valid_keys -= kChunkN / 2 * H;
+  const bool all_valid = valid_keys >= kChunkN / 2;
+  static_assert(ITER % 8 == 0, "each half is a whole number of four-key batches");
 #pragma unroll
-  for (int i0 = 0; i0 < ITER; i0 += 4) {
+  for (int i0 = 0; i0 < ITER / 2; i0 += 4) {
     uint4 w[4];
     uint32_t s2[4];
 #pragma unroll
@@ -602,34 +615,73 @@ __device__ __forceinline__ void dequant_tile(const uint8_t* __restrict__ raw_q, 
   }
 }
 
+// One out-of-line copy per format serves both key halves and both operands: the
+// dequant code of the K and V groups then shares instruction-cache lines.  The
+// fp16 "dequantisation" (a swizzled copy) stays inline.
+template <int F, int D, bool LO>
+__device__ __noinline__ void dequant_half_call(const uint8_t* __restrict__ raw_q, const uint8_t* __restrict__ raw_s,
+                                               uint8_t* __restrict__ dst_hi, uint8_t* __restrict__ dst_lo,
+                                               int valid_keys, int t0, int H) {
+  dequant_half_body<F, D, LO>(raw_q, raw_s, dst_hi, dst_lo, valid_keys, t0, H);
+}
+
+template <int F, int D, bool LO>
+__device__ __forceinline__ void dequant_half(const uint8_t* raw_q, const uint8_t* raw_s, uint8_t* dst_hi,
+                                             uint8_t* dst_lo, int valid_keys, int t0, int H) {
+  if constexpr (F == MIXATTN_KV_F16)
+    dequant_half_body<F, D, LO>(raw_q, raw_s, dst_hi, dst_lo, valid_keys, t0, H);
+  else
+    dequant_half_call<F, D, LO>(raw_q, raw_s, dst_hi, dst_lo, valid_keys, t0, H);
+}
+
 // Chunk tile: 128 rows (128/G query tokens x G heads of kv head `t.kvh`) against
-// the keys they can see, in 128-key KV tiles j, by two groups of 4 warps:
-//   dequant group (warps 4-7): waits for raw tile j (bulk copies, two stages),
-//     dequantises K(j) once QK(j-1) has released the K tiles, issues QK(j) into
-//     S[j%2] (TMEM), dequantises V(j) once PV(j-1) has released the V tiles,
-//     signals vdeq_done, refills the raw stage with tile j+2;
-//   softmax group (warps 0-3, thread i = TMEM lane i = query row i): turns
-//     S[j%2] into P (fp16, written over the scores), waits for PV(j-1), rescales
-//     O when the row max moved, then issues PV(j).
+// the keys they can see, in 128-key KV tiles j.  Each K and V operand tile is
+// handled as two 64-key halves, so the dequantisation of tile j+1 overlaps the
+// MMAs of tile j half by half.  Roles:
+//   K producer (warp 13, one thread) and V producer (warp 14, one thread): bulk
+//     copies of the raw K (V) pages of tile j into a ring of raw stages, each
+//     stage refilled once its dequant group is done with it; the page ids are
+//     fetched one tile ahead;
+//   K group (warps 4-7): dequantises the upper, then the lower key half of K(j),
+//     each once QK of tile j-1 has released that half;
+//   V group (warps 8-11): the same for V(j) against the two halves of PV(j-1);
+//   softmax group (warps 0-3, thread i = TMEM lane i = query row i): reads
+//     S[j%2] twice (row max, then P = 2^(s - m) as fp16 written over the
+//     scores), waits for PV(j-1), rescales O when the row max moved;
+//   MMA warp (warp 12, one thread): issues QK(j) into S[j%2] (upper key half
+//     first: P(j-2) lives in the lower 64 columns until PV(j-2) has read it),
+//     then PV(j-1), each half as soon as its operand half is ready.
 // TMEM: Q (A operand, fp16) | S0 | S1 | O (fp32).  Every wait is bounded; a
-// timeout in either group makes both leave their loops.
+// timeout in any role makes all of them leave their loops.
 template <int FK, int FV, int D>
 __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& t, uint8_t* smem_raw,
                                            unsigned int* err) {
   using L = ChunkSmem<FK, FV, D>;
-  constexpr int NB = D / kBlock;
+  constexpr int NKS = L::kKStages, NVS = L::kVStages;
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kQCol = 0, kSCol0 = 128, kSCol1 = 256, kOCol = 384;
-  constexpr int kGroup = 128;  // threads per group
-  constexpr int kBarSoftmax = 1, kBarDequant = 2;
+  constexpr int kGroup = 128;          // threads per warp group
+  constexpr int kHalfN = kChunkN / 2;  // keys per operand half
+  constexpr int kBarSoftmax = 1, kBarK = 2, kBarV = 3;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + L::kBar);  // [2]
-  uint64_t* qk_done = raw_full + 2;                                  // [2]
-  uint64_t* pv_done = raw_full + 4;                                  // [2]
-  uint64_t* vdeq_done = raw_full + 6;                                // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(raw_full + 8);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(raw_full + 9);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* k_full = bars;                 // [NKS] raw K stage landed
+  uint64_t* k_free = k_full + NKS;         // [NKS] raw K stage consumed
+  uint64_t* v_full = k_free + NKS;         // [NVS]
+  uint64_t* v_free = v_full + NVS;         // [NVS]
+  uint64_t* kdeq = v_free + NVS;           // [2] K half h of the current tile written
+  uint64_t* vdeq = kdeq + 2;               // [2] V half h written
+  uint64_t* qkh_done = vdeq + 2;           // [2] the QK MMAs reading K half h are done
+  uint64_t* pvh_done = qkh_done + 2;       // [2] the PV MMAs reading V half h are done
+  uint64_t* qk_done = pvh_done + 2;        // [2] S[st] holds the scores of the tile
+  uint64_t* pv_done = qk_done + 2;         // [2] PV of the tile done (P in S[st] read)
+  uint64_t* sm_done = pv_done + 2;         // [2] P of the tile written, O rescaled
+  uint64_t* mma_fin = sm_done + 2;         // [1] every MMA of the tile done
+  constexpr int kNumBars = 2 * NKS + 2 * NVS + 15;
+  static_assert(kNumBars * 8 + 8 <= L::kBarBytes, "barrier area too small");
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kNumBars) + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int G = p.group, lg = p.log2_group;
@@ -642,8 +694,7 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
   const int32_t* pt_row = p.page_table + (int64_t)t.row * p.max_pages;
 
   if (tid == 0) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) mbar_init(raw_full + i, 1);
+    for (int i = 0; i < kNumBars; ++i) mbar_init(bars + i, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -687,185 +738,140 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
   __syncthreads();
   tc_fence_after();
 
-  // ---- producer: raw pages of KV tile jj into stage st ----
-  auto issue_raw = [&](int jj, int st) {
-    uint8_t* raw = smem + L::kRaw + st * L::kRawBytes;
-    uint32_t bytes = 0;
-    int pids[L::kPagesPerTile];
-#pragma unroll
-    for (int pj = 0; pj < L::kPagesPerTile; ++pj) {
-      const int pg = jj * L::kPagesPerTile + pj;
-      int pid = -1;
-      if (pg < n_pages_row && pg * kPage < key_end) {
-        pid = pt_row[pg];
-        if (pid < 0 || pid >= p.num_pages) {
-          set_device_error(err, MIXATTN_DEVERR_PAGE_ID);
-          pid = -1;
-        }
-      }
-      pids[pj] = pid;
-      if (pid >= 0) bytes += L::kKqPage + L::kKsPage + L::kVqPage + L::kVsPage;
-    }
-    mbar_arrive_expect_tx(&raw_full[st], bytes);
-#pragma unroll
-    for (int pj = 0; pj < L::kPagesPerTile; ++pj) {
-      const int pid = pids[pj];
-      if (pid < 0) continue;
-      const int64_t prow = ((int64_t)pid * p.hkv + g) * kPage;  // first plane row of (page, head)
-      bulk_g2s(raw + L::kRawKq + pj * L::kKqPage, p.k_quant + prow * (L::kKqPage / kPage), L::kKqPage,
-               &raw_full[st]);
-      if (L::kKsPage)
-        bulk_g2s(raw + L::kRawKs + pj * L::kKsPage, p.k_scale + prow * NB, L::kKsPage, &raw_full[st]);
-      bulk_g2s(raw + L::kRawVq + pj * L::kVqPage, p.v_quant + prow * (L::kVqPage / kPage), L::kVqPage,
-               &raw_full[st]);
-      if (L::kVsPage)
-        bulk_g2s(raw + L::kRawVs + pj * L::kVsPage, p.v_scale + prow * NB, L::kVsPage, &raw_full[st]);
-    }
-  };
-
-  constexpr uint32_t kIdescQK = idesc_f16_f32(128, kChunkN, false, false);
+  constexpr uint32_t kIdescQK = idesc_f16_f32(128, kHalfN, false, false);
   constexpr uint32_t kIdescPV = idesc_f16_f32(128, D, false, true);
   const uint32_t sKh = smem_u32(smem + L::kKh), sKl = smem_u32(smem + L::kKl);
   const uint32_t sVh = smem_u32(smem + L::kVh), sVl = smem_u32(smem + L::kVl);
   bool ok = true;
-  int qk_issued = 0, pv_issued = 0, raw_issued = 0;
   float m_run = -CUDART_INF_F, l_run = 0.f;
 
-  if (tid >= kGroup) {
-    // ======================= dequant group =======================
+  if (tid >= kGroup && tid < 2 * kGroup) {
+    // ======================= K group (warps 4-7) =======================
     const int dt = tid - kGroup;
-    if (dt == 0) {
-      for (int jj = 0; jj < 2 && jj < n_kv; ++jj) issue_raw(jj, jj);
-      raw_issued = min(2, n_kv);
-    }
     for (int j = 0; j < n_kv; ++j) {
-      const int st = j & 1;
-      const uint32_t ph = (uint32_t)((j >> 1) & 1), ph_prev = (uint32_t)(((j - 1) >> 1) & 1);
-      ok = mbar_wait(&raw_full[st], ph, err) && ok;
-      if (j > 0) ok = mbar_wait(&qk_done[(j - 1) & 1], ph_prev, err) && ok;  // K tiles free
-      tc_fence_after();
-      const uint8_t* raw = smem + L::kRaw + st * L::kRawBytes;
+      const int rs = j % NKS;
+      const uint32_t ph_prev = (uint32_t)((j - 1) & 1);
+      ok = mbar_wait(&k_full[rs], (uint32_t)((j / NKS) & 1), err) && ok;
+      const uint8_t* raw = smem + L::kKRaw + rs * L::kKRawBytes;
       const int valid_keys = key_end - j * kChunkN;
-      dequant_tile<FK, D, L::kKLo>(raw + L::kRawKq, raw + L::kRawKs, smem + L::kKh, smem + L::kKl, valid_keys, dt);
-      fence_proxy_async_smem();
-      if (bar_any(kBarDequant, kGroup, !ok || *abort_flag)) {  // one decision for the group
-        *abort_flag = 1;
-        break;
-      }
-      if (dt == 0) {
-        tc_fence_after();
-        const uint32_t s_col = st ? kSCol1 : kSCol0;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (uint32_t)((ks >> 2) * (kChunkN * 128) + (ks & 3) * 32);
-          tc_mma_ts(tmem + s_col, tmem + kQCol + 8 * ks, sw128_desc(sKh + off, 16, 1024), kIdescQK,
-                    ks > 0 ? 1u : 0u);
-          if (L::kKLo) tc_mma_ts(tmem + s_col, tmem + kQCol + 8 * ks, sw128_desc(sKl + off, 16, 1024), kIdescQK, 1u);
-        }
-        tc_commit(&qk_done[st]);
-        ++qk_issued;
-      }
-      if (j > 0) ok = mbar_wait(&pv_done[(j - 1) & 1], ph_prev, err) && ok;  // V tiles free
+      // the upper key half first: the MMA warp issues its QK half first
+      if (j > 0) ok = mbar_wait(&qkh_done[1], ph_prev, err) && ok;
       tc_fence_after();
-      dequant_tile<FV, D, L::kVLo>(raw + L::kRawVq, raw + L::kRawVs, smem + L::kVh, smem + L::kVl, valid_keys, dt);
+      dequant_half<FK, D, L::kKLo>(raw, raw + L::kKsOff, smem + L::kKh, smem + L::kKl, valid_keys, dt, 1);
       fence_proxy_async_smem();
-      if (bar_any(kBarDequant, kGroup, !ok || *abort_flag)) {  // one decision for the group
+      if (bar_any(kBarK, kGroup, !ok || *abort_flag)) {  // one decision for the group
+        *abort_flag = 1;
+        break;
+      }
+      if (dt == 0) mbar_arrive(&kdeq[1]);
+      if (j > 0) ok = mbar_wait(&qkh_done[0], ph_prev, err) && ok;
+      tc_fence_after();
+      dequant_half<FK, D, L::kKLo>(raw, raw + L::kKsOff, smem + L::kKh, smem + L::kKl, valid_keys, dt, 0);
+      fence_proxy_async_smem();
+      if (bar_any(kBarK, kGroup, !ok || *abort_flag)) {
         *abort_flag = 1;
         break;
       }
       if (dt == 0) {
-        mbar_arrive(&vdeq_done[st]);
-        if (j + 2 < n_kv) {  // the stage is consumed: refill it with tile j+2
-          issue_raw(j + 2, st);
-          raw_issued = j + 3;
-        }
+        mbar_arrive(&kdeq[0]);
+        mbar_arrive(&k_free[rs]);  // the raw K stage may be refilled
       }
     }
-    if (dt == 0) {
-      // nothing this group started may still run when TMEM and the stages are released
-      if (qk_issued > 0) mbar_wait(&qk_done[(qk_issued - 1) & 1], (uint32_t)(((qk_issued - 1) >> 1) & 1), err);
-      for (int jj = max(0, raw_issued - 2); jj < raw_issued; ++jj)
-        mbar_wait(&raw_full[jj & 1], (uint32_t)((jj >> 1) & 1), err);
+  } else if (tid >= 2 * kGroup && tid < 3 * kGroup) {
+    // ======================= V group (warps 8-11) =======================
+    const int dt = tid - 2 * kGroup;
+    for (int j = 0; j < n_kv; ++j) {
+      const int rs = j % NVS;
+      const uint32_t ph_prev = (uint32_t)((j - 1) & 1);
+      ok = mbar_wait(&v_full[rs], (uint32_t)((j / NVS) & 1), err) && ok;
+      const uint8_t* raw = smem + L::kVRaw + rs * L::kVRawBytes;
+      const int valid_keys = key_end - j * kChunkN;
+      // the lower key half first: PV reads it first
+      if (j > 0) ok = mbar_wait(&pvh_done[0], ph_prev, err) && ok;
+      tc_fence_after();
+      dequant_half<FV, D, L::kVLo>(raw, raw + L::kVsOff, smem + L::kVh, smem + L::kVl, valid_keys, dt, 0);
+      fence_proxy_async_smem();
+      if (bar_any(kBarV, kGroup, !ok || *abort_flag)) {
+        *abort_flag = 1;
+        break;
+      }
+      if (dt == 0) mbar_arrive(&vdeq[0]);
+      if (j > 0) ok = mbar_wait(&pvh_done[1], ph_prev, err) && ok;
+      tc_fence_after();
+      dequant_half<FV, D, L::kVLo>(raw, raw + L::kVsOff, smem + L::kVh, smem + L::kVl, valid_keys, dt, 1);
+      fence_proxy_async_smem();
+      if (bar_any(kBarV, kGroup, !ok || *abort_flag)) {
+        *abort_flag = 1;
+        break;
+      }
+      if (dt == 0) {
+        mbar_arrive(&vdeq[1]);
+        mbar_arrive(&v_free[rs]);
+      }
     }
-  } else {
+  } else if (tid < kGroup) {
     // ======================= softmax group =======================
     const float sl2 = p.scale_log2;
+    const uint32_t ninf = __float_as_uint(-CUDART_INF_F);
     for (int j = 0; j < n_kv; ++j) {
       const int st = j & 1;
       const uint32_t ph = (uint32_t)((j >> 1) & 1), ph_prev = (uint32_t)(((j - 1) >> 1) & 1);
-      const uint32_t s_col = st ? kSCol1 : kSCol0;
+      const uint32_t s_base = st ? kSCol1 : kSCol0;
+      const uint32_t s_col = tmem + lane_base + s_base;
       ok = mbar_wait(&qk_done[st], ph, err) && ok;
       tc_fence_after();
       const int kbase = j * kChunkN;
-      // the tile's 128 scores of this row, held in registers (one TMEM read)
-      uint32_t v0[32], v1[32], v2[32], v3[32];
-      tmem_ld32(tmem + lane_base + s_col + 0, v0);
-      tmem_ld32(tmem + lane_base + s_col + 32, v1);
-      tmem_ld32(tmem + lane_base + s_col + 64, v2);
-      tmem_ld32(tmem + lane_base + s_col + 96, v3);
-      tmem_wait_ld();
       // causal mask: only a warp whose tile crosses the diagonal pays for it
-      if (__any_sync(0xFFFFFFFFu, kbase + kChunkN - 1 > pos)) {
-        const uint32_t ninf = __float_as_uint(-CUDART_INF_F);
+      const bool diag = __any_sync(0xFFFFFFFFu, kbase + kChunkN - 1 > pos);
+      uint32_t a[32];
+      // pass 1: the row max of the tile's 128 scores, 32 at a time
+      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(s_col + 32 * c, a);
+        tmem_wait_ld();
+        if (diag) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          if (kbase + e > pos) v0[e] = ninf;
-          if (kbase + 32 + e > pos) v1[e] = ninf;
-          if (kbase + 64 + e > pos) v2[e] = ninf;
-          if (kbase + 96 + e > pos) v3[e] = ninf;
+          for (int e = 0; e < 32; ++e)
+            if (kbase + 32 * c + e > pos) a[e] = ninf;
         }
-      }
-      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        mx0 = fmaxf(mx0, __uint_as_float(v0[e]));
-        mx1 = fmaxf(mx1, __uint_as_float(v1[e]));
-        mx2 = fmaxf(mx2, __uint_as_float(v2[e]));
-        mx3 = fmaxf(mx3, __uint_as_float(v3[e]));
+        for (int e = 0; e < 32; e += 2) {
+          mx0 = fmaxf(mx0, __uint_as_float(a[e]));
+          mx1 = fmaxf(mx1, __uint_as_float(a[e + 1]));
+        }
       }
       // running max in log2 units (the score scale is positive, so it commutes with max)
-      const float m_new = fmaxf(m_run, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+      const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * sl2);
       const float alpha = ex2(m_run - m_new);
       const float neg_m = -m_new;
-      // P = 2^(s*scale - m) as fp16 into TMEM over the consumed scores; row sums
-      float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
-      {
+      // pass 2: P = 2^(s*scale - m) as fp16 over the consumed scores (chunk c of
+      // P lands on columns of chunks already read); row sums in fp32
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(s_col + 32 * c, a);
+        tmem_wait_ld();
+        if (diag) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (kbase + 32 * c + e > pos) a[e] = ninf;
+        }
         uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float a0 = ex2(fmaf(__uint_as_float(v0[e]), sl2, neg_m));
-          const float a1 = ex2(fmaf(__uint_as_float(v0[e + 1]), sl2, neg_m));
+        for (int e = 0; e < 32; e += 4) {
+          const float a0 = ex2(fmaf(__uint_as_float(a[e]), sl2, neg_m));
+          const float a1 = ex2(fmaf(__uint_as_float(a[e + 1]), sl2, neg_m));
+          const float a2 = ex2(fmaf(__uint_as_float(a[e + 2]), sl2, neg_m));
+          const float a3 = ex2(fmaf(__uint_as_float(a[e + 3]), sl2, neg_m));
           sum0 += a0 + a1;
+          sum1 += a2 + a3;
           pk[e >> 1] = pack_f16x2(a0, a1);
+          pk[(e >> 1) + 1] = pack_f16x2(a2, a3);
         }
-        tmem_st16(tmem + lane_base + s_col + 0, pk);
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float a0 = ex2(fmaf(__uint_as_float(v1[e]), sl2, neg_m));
-          const float a1 = ex2(fmaf(__uint_as_float(v1[e + 1]), sl2, neg_m));
-          sum1 += a0 + a1;
-          pk[e >> 1] = pack_f16x2(a0, a1);
-        }
-        tmem_st16(tmem + lane_base + s_col + 16, pk);
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float a0 = ex2(fmaf(__uint_as_float(v2[e]), sl2, neg_m));
-          const float a1 = ex2(fmaf(__uint_as_float(v2[e + 1]), sl2, neg_m));
-          sum2 += a0 + a1;
-          pk[e >> 1] = pack_f16x2(a0, a1);
-        }
-        tmem_st16(tmem + lane_base + s_col + 32, pk);
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float a0 = ex2(fmaf(__uint_as_float(v3[e]), sl2, neg_m));
-          const float a1 = ex2(fmaf(__uint_as_float(v3[e + 1]), sl2, neg_m));
-          sum3 += a0 + a1;
-          pk[e >> 1] = pack_f16x2(a0, a1);
-        }
-        tmem_st16(tmem + lane_base + s_col + 48, pk);
+        tmem_st16(s_col + 16 * c, pk);
       }
-      const float sum = (sum0 + sum1) + (sum2 + sum3);
-      l_run = l_run * alpha + sum;
+      l_run = l_run * alpha + (sum0 + sum1);
       m_run = m_new;
       // the running O may be rescaled only once PV(j-1) has finished with it
       if (j > 0) {
@@ -874,12 +880,11 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
         if (__any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
 #pragma unroll 1
           for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_base + kOCol + 32 * ch, v);
+            tmem_ld32(tmem + lane_base + kOCol + 32 * ch, a);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tmem_st32(tmem + lane_base + kOCol + 32 * ch, v);
+            for (int e = 0; e < 32; ++e) a[e] = __float_as_uint(__uint_as_float(a[e]) * alpha);
+            tmem_st32(tmem + lane_base + kOCol + 32 * ch, a);
           }
         }
       }
@@ -889,24 +894,10 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
         *abort_flag = 1;
         break;
       }
-      if (tid == 0) {
-        ok = mbar_wait(&vdeq_done[st], ph, err) && ok;  // V(j) tiles written
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kChunkN / 16; ++kk) {
-          const uint32_t pa = tmem + s_col + 8 * kk;  // P columns of keys 16kk..16kk+15
-          const uint32_t boff = (uint32_t)(kk * 16 * 128);
-          const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-          tc_mma_ts(tmem + kOCol, pa, sw128_desc(sVh + boff, kChunkN * 128, 1024), kIdescPV, acc);
-          if (L::kVLo) tc_mma_ts(tmem + kOCol, pa, sw128_desc(sVl + boff, kChunkN * 128, 1024), kIdescPV, 1u);
-        }
-        tc_commit(&pv_done[st]);
-        ++pv_issued;
-      }
+      if (tid == 0) mbar_arrive(&sm_done[st]);  // P(j) written, O rescaled
     }
     // ---- epilogue: O / l -> fp16 ----
     const bool done = !*abort_flag;
-    if (tid == 0 && pv_issued > 0) mbar_wait(&pv_done[(pv_issued - 1) & 1], (uint32_t)(((pv_issued - 1) >> 1) & 1), err);
     if (done) ok = mbar_wait(&pv_done[(n_kv - 1) & 1], (uint32_t)(((n_kv - 1) >> 1) & 1), err) && ok;
     tc_fence_after();
     const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
@@ -928,6 +919,124 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
               make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
       }
     }
+  } else if (tid == 3 * kGroup) {
+    // ============ MMA warp (warp 12, one thread): issues every tcgen05.mma ============
+    // Order on the tensor pipe: QK(0), QK(1), PV(0), QK(2), PV(1), ...
+    for (int j = 0; j <= n_kv; ++j) {
+      if (j < n_kv) {
+        const int st = j & 1;
+        const uint32_t s_col = tmem + (st ? kSCol1 : kSCol0);
+#pragma unroll
+        for (int hf = 1; hf >= 0; --hf) {
+          ok = mbar_wait(&kdeq[hf], (uint32_t)(j & 1), err) && ok;  // K half hf of tile j written
+          // the lower 64 columns of S[st] hold P(j-2) until PV(j-2) has read it
+          if (hf == 0 && j > 1) ok = mbar_wait(&pv_done[st], (uint32_t)(((j - 2) >> 1) & 1), err) && ok;
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (uint32_t)((ks >> 2) * (kChunkN * 128) + (ks & 3) * 32 + hf * (kHalfN * 128));
+            tc_mma_ts(s_col + hf * kHalfN, tmem + kQCol + 8 * ks, sw128_desc(sKh + off, 16, 1024), kIdescQK,
+                      ks > 0 ? 1u : 0u);
+            if (L::kKLo)
+              tc_mma_ts(s_col + hf * kHalfN, tmem + kQCol + 8 * ks, sw128_desc(sKl + off, 16, 1024), kIdescQK, 1u);
+          }
+          tc_commit(&qkh_done[hf]);
+        }
+        if (!ok) break;
+        tc_commit(&qk_done[st]);
+      }
+      if (j > 0) {
+        const int jp = j - 1, sp = jp & 1;
+        ok = mbar_wait(&sm_done[sp], (uint32_t)((jp >> 1) & 1), err) && ok;  // P(j-1) written, O rescaled
+        const uint32_t p_col = tmem + (sp ? kSCol1 : kSCol0);
+#pragma unroll
+        for (int hv = 0; hv < 2; ++hv) {
+          ok = mbar_wait(&vdeq[hv], (uint32_t)(jp & 1), err) && ok;  // V half hv of tile j-1 written
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 4 * hv; kk < 4 * hv + 4; ++kk) {
+            const uint32_t pa = p_col + 8 * kk;  // P columns of keys 16kk..16kk+15
+            const uint32_t boff = (uint32_t)(kk * 16 * 128);
+            const uint32_t acc = (jp > 0 || kk > 0) ? 1u : 0u;
+            tc_mma_ts(tmem + kOCol, pa, sw128_desc(sVh + boff, kChunkN * 128, 1024), kIdescPV, acc);
+            if (L::kVLo) tc_mma_ts(tmem + kOCol, pa, sw128_desc(sVl + boff, kChunkN * 128, 1024), kIdescPV, 1u);
+          }
+          tc_commit(&pvh_done[hv]);
+        }
+        if (!ok) break;
+        tc_commit(&pv_done[sp]);
+      }
+      if (*abort_flag) break;
+    }
+    if (!ok) *abort_flag = 1;
+    // nothing this thread started may still run when TMEM is released
+    tc_commit(mma_fin);
+    mbar_wait(mma_fin, 0u, err);
+  } else if (tid == 3 * kGroup + 32 || tid == 3 * kGroup + 64) {
+    // ===== producers (warps 13 and 14, one thread each): raw K / raw V pages of tile j =====
+    const bool is_k = tid == 3 * kGroup + 32;
+    const int ns = is_k ? NKS : NVS;
+    uint64_t* full = is_k ? k_full : v_full;
+    uint64_t* free_ = is_k ? k_free : v_free;
+    uint8_t* ring = smem + (is_k ? L::kKRaw : L::kVRaw);
+    const int stage_bytes = is_k ? L::kKRawBytes : L::kVRawBytes;
+    const int q_page = is_k ? L::kKqPage : L::kVqPage, s_page = is_k ? L::kKsPage : L::kVsPage;
+    const int s_off = is_k ? L::kKsOff : L::kVsOff;
+    const uint8_t* q_src = is_k ? p.k_quant : p.v_quant;
+    const uint8_t* s_src = reinterpret_cast<const uint8_t*>(is_k ? p.k_scale : p.v_scale);
+    int pids[L::kPagesPerTile];
+    // page ids of tile jj (validated; -1 = no page: keys past the tile's end)
+    auto load_pids = [&](int jj) {
+#pragma unroll
+      for (int pj = 0; pj < L::kPagesPerTile; ++pj) {
+        const int pg = jj * L::kPagesPerTile + pj;
+        int pid = -1;
+        if (pg < n_pages_row && pg * kPage < key_end) {
+          pid = pt_row[pg];
+          if (pid < 0 || pid >= p.num_pages) {
+            set_device_error(err, MIXATTN_DEVERR_PAGE_ID);
+            pid = -1;
+          }
+        }
+        pids[pj] = pid;
+      }
+    };
+    auto issue = [&](int s) {
+      uint8_t* raw = ring + s * stage_bytes;
+      uint32_t bytes = 0;
+#pragma unroll
+      for (int pj = 0; pj < L::kPagesPerTile; ++pj)
+        if (pids[pj] >= 0) bytes += q_page + s_page;
+      mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll
+      for (int pj = 0; pj < L::kPagesPerTile; ++pj) {
+        if (pids[pj] < 0) continue;
+        const int64_t prow = ((int64_t)pids[pj] * p.hkv + g) * kPage;  // first plane row of (page, head)
+        bulk_g2s(raw + pj * q_page, q_src + prow * (q_page / kPage), q_page, &full[s]);
+        if (s_page) bulk_g2s(raw + s_off + pj * s_page, s_src + prow * (s_page / kPage), s_page, &full[s]);
+      }
+    };
+    int issued = 0;
+    for (; issued < ns && issued < n_kv; ++issued) {
+      load_pids(issued);
+      issue(issued);
+    }
+    if (issued < n_kv) load_pids(issued);  // one tile ahead
+    for (int j = 0; issued < n_kv; ++j) {
+      // stage j%ns is free once its dequant group is done with tile j
+      const int rs = j % ns;
+      ok = mbar_wait(&free_[rs], (uint32_t)((j / ns) & 1), err) && ok;
+      if (!ok || *abort_flag) break;
+      issue(rs);
+      ++issued;
+      if (issued < n_kv) load_pids(issued);
+    }
+    if (!ok) *abort_flag = 1;
+    // no copy this thread started may still land when the stages are released
+    for (int jj = max(0, issued - ns); jj < issued; ++jj)
+      mbar_wait(&full[jj % ns], (uint32_t)((jj / ns) & 1), err);
   }
   tc_fence_before();
   __syncthreads();
@@ -947,12 +1056,13 @@ struct FusedSmem {
 };
 
 template <int FK, int FV, int D>
-__global__ void __launch_bounds__(kThreads, 1) mixed_attention_kernel(AttnParams p, unsigned int* err) {
+__global__ void __launch_bounds__(kFusedThreads, 1) mixed_attention_kernel(AttnParams p, unsigned int* err) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tile = blockIdx.x;
   if (tile < p.n_chunk_tiles) {
     chunk_tile<FK, FV, D>(p, p.tiles[tile], smem, err);
   } else {
+    if (threadIdx.x >= kThreads) return;  // a decode tile runs on 8 warps
     decode_tile<FK, FV, D, FusedSmem<FK, FV, D>::kDecodeStages>(p, p.tiles[tile], tile - p.n_chunk_tiles, smem,
                                                                err);
   }
@@ -985,7 +1095,7 @@ cudaError_t launch_attention_t(const AttnParams& p, unsigned int* err, cudaStrea
   if (p.n_chunk_tiles == 0) {
     dec_kernel<<<p.n_decode_tiles, kThreads, kDec, s>>>(p, err);
   } else {
-    mixed_attention_kernel<FK, FV, D><<<n_tiles, kThreads, kFused, s>>>(p, err);
+    mixed_attention_kernel<FK, FV, D><<<n_tiles, kFusedThreads, kFused, s>>>(p, err);
   }
   return cudaGetLastError();
 }

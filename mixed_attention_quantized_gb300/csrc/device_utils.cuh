@@ -40,6 +40,12 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   return r;
 }
 
+__device__ __forceinline__ uint32_t hneg2_u32(uint32_t a) {
+  uint32_t r;
+  asm("neg.f16x2 %0, %1;" : "=r"(r) : "r"(a));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t r;
   asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));

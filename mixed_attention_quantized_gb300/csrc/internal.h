@@ -20,8 +20,11 @@ namespace mixattn {
 
 constexpr int kPage = 32;          // tokens per page (the cache's page_size)
 constexpr int kBlock = 32;         // elements per quantisation block
-constexpr int kThreads = 256;      // threads of every attention CTA (8 warps)
+constexpr int kThreads = 256;      // threads of a decode CTA (8 warps)
 constexpr int kWarps = kThreads / 32;
+constexpr int kFusedThreads = 512; // threads of a fused-launch CTA: three working warp groups and
+                                   // an MMA/producer group on a chunk tile; a decode tile uses
+                                   // the first kThreads
 constexpr int kChunkM = 128;       // rows (query tokens x group heads) of a chunk tile
 constexpr int kChunkN = 128;       // keys per KV tile of the chunk path (4 pages)
 constexpr int kMaxGroup = 8;       // q heads per kv head held in one mma N=8 tile
