@@ -43,33 +43,17 @@ namespace mixattn {
 // ===========================================================================
 template <int FK, int FV, int D>
 struct ChunkSmem {
-  static constexpr int kNb = D / kBlock;
-  static constexpr int kKqPage = kPage * (FK == MIXATTN_KV_F16 ? 2 * D : (FK == MIXATTN_KV_Q8_0 ? D : D / 2));
-  static constexpr int kKsPage = FK == MIXATTN_KV_F16 ? 0 : kPage * kNb * 2;
-  static constexpr int kVqPage = kPage * (FV == MIXATTN_KV_F16 ? 2 * D : (FV == MIXATTN_KV_Q8_0 ? D : D / 2));
-  static constexpr int kVsPage = FV == MIXATTN_KV_F16 ? 0 : kPage * kNb * 2;
-  static constexpr int kPagesPerTile = kChunkN / kPage;  // 4
   // quantised formats carry an exact low half: d*q = hi + lo, both fp16
   static constexpr bool kKLo = FK != MIXATTN_KV_F16;
   static constexpr bool kVLo = FV != MIXATTN_KV_F16;
-  static constexpr int kTile = kChunkN * D * 2;             // one fp16 operand tile
-  static constexpr int kKh = 0;                             // [D/64][128 keys][128 B]
-  static constexpr int kKl = kKh + kTile;
-  static constexpr int kVh = kKl + (kKLo ? kTile : 0);
+  static constexpr int kTile = kChunkN * D * 2;             // one fp16 operand tile [D/64][128 keys][128 B]
+  static constexpr int kKBuf = kTile * (kKLo ? 2 : 1);      // one K buffer: hi (+ lo)
+  static constexpr int kK0 = 0;                             // K(j) lives in buffer j % 2
+  static constexpr int kK1 = kKBuf;
+  static constexpr int kVh = 2 * kKBuf;
   static constexpr int kVl = kVh + kTile;
-  // raw K stage: [Kq x4][Ks x4]; raw V stage: [Vq x4][Vs x4]
-  static constexpr int kKsOff = kPagesPerTile * kKqPage;
-  static constexpr int kVsOff = kPagesPerTile * kVqPage;
-  static constexpr int kKRawBytes = (kKsOff + kPagesPerTile * kKsPage + 1023) / 1024 * 1024;
-  static constexpr int kVRawBytes = (kVsOff + kPagesPerTile * kVsPage + 1023) / 1024 * 1024;
-  static constexpr int kBarBytes = 256;                     // mbarriers, TMEM address, abort flag
-  static constexpr int kRawBudget = 227 * 1024 - 1024 - kBarBytes - (kVl + (kVLo ? kTile : 0));
-  // three raw K stages where they fit (K is dequantised first), then three raw V stages
-  static constexpr int kKStages = 3 * kKRawBytes + 2 * kVRawBytes <= kRawBudget ? 3 : 2;
-  static constexpr int kVStages = kKStages * kKRawBytes + 3 * kVRawBytes <= kRawBudget ? 3 : 2;
-  static constexpr int kKRaw = kVl + (kVLo ? kTile : 0);
-  static constexpr int kVRaw = kKRaw + kKStages * kKRawBytes;
-  static constexpr int kBar = kVRaw + kVStages * kVRawBytes;
+  static constexpr int kBar = kVl + (kVLo ? kTile : 0);
+  static constexpr int kBarBytes = 128;                     // mbarriers, TMEM address, abort flag
   static constexpr int kTotal = kBar + kBarBytes + 1024;   // + slack for 1024-B alignment
   static_assert(kTotal <= 227 * 1024, "chunk tile does not fit in shared memory");
 };
@@ -535,150 +519,206 @@ __device__ __forceinline__ void split_hilo(uint32_t v, uint32_t s, uint32_t& hi,
   lo = hfma2_u32(v, s, hneg2_u32(hi));  // the negation folds into the fma
 }
 
-// Dequantise key half H (keys 64H..64H+63) of one 128-key x D tile from a raw
-// stage into swizzled fp16 tiles (hi, and lo for quantised formats), by the 128
-// threads numbered t0 = 0..127.
-// Keys at or past `valid_keys` (relative to the tile) are written as zeros.
-//
-// Thread t0 owns one 16-byte output column chunk (dc = t0 % (D/8)) and the keys
-// t0 / (D/8) + i * KPI.  The raw stage holds the tile's 4 pages back to back,
-// so the source row of a key is raw + key * row_bytes; KPI is a multiple of 8,
-// so the swizzle term (key & 7) is fixed per thread and every address is a
-// base plus i times a constant.  Loads for four keys are issued before any
-// conversion.
-template <int F, int D, bool LO>
-__device__ __forceinline__ void dequant_half_body(const uint8_t* __restrict__ raw_q, const uint8_t* __restrict__ raw_s,
-                                             uint8_t* __restrict__ dst_hi, uint8_t* __restrict__ dst_lo,
-                                                  int valid_keys, int t0, int H) {
-  constexpr int NB = D / kBlock;
-  constexpr int CPR = D / 8;           // 16-byte fp16 chunks per key row
-  constexpr int KPI = 128 / CPR;       // keys advanced per step (8 or 16)
-  constexpr int ITER = kChunkN / KPI;  // steps per thread (16 or 8)
-  constexpr int RB = F == MIXATTN_KV_F16 ? 2 * D : (F == MIXATTN_KV_Q8_0 ? D : D / 2);
-  static_assert(KPI % 8 == 0, "the swizzle phase must be fixed per thread");
-  const int dc = t0 % CPR, key0 = t0 / CPR;
-  const int b = dc >> 2, half = dc >> 3, cc = dc & 7;
+// Dequantisation of the chunk path.  Thread t0 (0..127) of a dequant group owns
+// one 16-byte output column chunk, dc = t0 % (D/8), of the keys
+// key0 + i * KPI, key0 = t0 / (D/8): KPI is a multiple of 8, so the swizzle term
+// (key & 7) is fixed per thread.  A key half (64 keys, pages 2h and 2h+1 of the
+// tile) gives each thread NH keys: the first NH/2 in page 2h, the rest in page
+// 2h+1.  Its raw bytes are loaded from the cache planes into registers one half
+// ahead of their conversion.
+template <int F, int D>
+struct DequantGeom {
+  static constexpr int NB = D / kBlock;
+  static constexpr int CPR = D / 8;                 // 16-byte fp16 chunks per key row
+  static constexpr int KPI = 128 / CPR;             // keys between a thread's keys (8 or 16)
+  static constexpr int NH = kChunkN / 2 / KPI;      // keys per thread per half (8 or 4)
+  static constexpr int RB = F == MIXATTN_KV_F16 ? 2 * D : (F == MIXATTN_KV_Q8_0 ? D : D / 2);  // row bytes
+  static_assert(KPI % 8 == 0 && NH % 2 == 0 && (NH / 2) * KPI == kPage, "key half layout");
+};
+
+constexpr int kNoPage = -2147483647 - 1;  // page id of a page past a row's key range
+
+// Raw bytes of one key half for one thread.
+template <int F, int D>
+struct HalfRaw {
+  static constexpr int NH = DequantGeom<F, D>::NH;
+  uint4 q[NH];     // fp16: the 8 values; Q8_0: 8 bytes in .x/.y; Q4_0: 8 bytes holding 16 nibbles
+  uint32_t s[NH];  // quantised formats: the block's fp16 scale (low 16 bits)
+};
+
+// Load the raw bytes of key half h of a tile for thread t0.  `pa`, `pb` are the
+// ids of the half's two pages (kNoPage: past the key range), `valid` the number of its keys that
+// exist (keys past it, and keys of a missing page, read as zeros).
+template <int F, int D>
+__device__ __forceinline__ void load_half(HalfRaw<F, D>& r, const uint8_t* __restrict__ q_plane,
+                                          const uint16_t* __restrict__ s_plane, int pa, int pb, int num_pages,
+                                          int hkv, int g, int valid, int t0, unsigned int* err) {
+  using Gm = DequantGeom<F, D>;
+  const int dc = t0 % Gm::CPR, key0 = t0 / Gm::CPR;
+  const int b = dc >> 2;
   int src_col;
   if (F == MIXATTN_KV_F16) src_col = 16 * dc;
   else if (F == MIXATTN_KV_Q8_0) src_col = 8 * dc;
   else src_col = 16 * b + 8 * (dc & 1);
-  const int shift = F == MIXATTN_KV_Q4_0 ? ((dc >> 1) & 1) * 4 : 0;  // low nibbles, then high nibbles
-  const int kh = key0 + kChunkN / 2 * H;  // first key of this thread in the half
-  const uint8_t* src = raw_q + kh * RB + src_col;
-  const uint8_t* ssrc = raw_s + kh * NB * 2 + 2 * b;
-  const uint32_t doff = (uint32_t)(half * (kChunkN * 128) + kh * 128 + ((cc ^ (key0 & 7)) << 4));
-  valid_keys -= kChunkN / 2 * H;
-  const bool all_valid = valid_keys >= kChunkN / 2;
-  static_assert(ITER % 8 == 0, "each half is a whole number of four-key batches");
+  const bool bad_a = pa != kNoPage && (pa < 0 || pa >= num_pages);
+  const bool bad_b = pb != kNoPage && (pb < 0 || pb >= num_pages);
+  if (bad_a || bad_b) {  // a page of the key range with an id outside the cache
+    set_device_error(err, MIXATTN_DEVERR_PAGE_ID);
+    if (bad_a) pa = kNoPage;
+    if (bad_b) pb = kNoPage;
+  }
 #pragma unroll
-  for (int i0 = 0; i0 < ITER / 2; i0 += 4) {
-    uint4 w[4];
-    uint32_t s2[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u;
-      if (F == MIXATTN_KV_F16) {
-        w[u] = *reinterpret_cast<const uint4*>(src + i * KPI * RB);
-      } else {
-        const uint2 x = *reinterpret_cast<const uint2*>(src + i * KPI * RB);
-        w[u] = make_uint4(x.x, x.y, 0u, 0u);
-        const uint32_t sh = *reinterpret_cast<const uint16_t*>(ssrc + i * KPI * NB * 2);
-        s2[u] = sh | (sh << 16);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u;
-      const bool valid = all_valid || key0 + i * KPI < valid_keys;
-      uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = make_uint4(0u, 0u, 0u, 0u);
-      if (valid) {
-        if (F == MIXATTN_KV_F16) {
-          hi = w[u];
-        } else {
-          uint32_t h0, h1, h2, h3;
-          if (F == MIXATTN_KV_Q8_0) {
-            s8x4_to_f16x2x2(w[u].x, h0, h1);
-            s8x4_to_f16x2x2(w[u].y, h2, h3);
-          } else {
-            u4x4_to_f16x2x2((w[u].x >> shift) & 0x0F0F0F0Fu, h0, h1);
-            u4x4_to_f16x2x2((w[u].y >> shift) & 0x0F0F0F0Fu, h2, h3);
-          }
-          split_hilo(h0, s2[u], hi.x, lo.x);
-          split_hilo(h1, s2[u], hi.y, lo.y);
-          split_hilo(h2, s2[u], hi.z, lo.z);
-          split_hilo(h3, s2[u], hi.w, lo.w);
-        }
-      }
-      *reinterpret_cast<uint4*>(dst_hi + doff + i * KPI * 128) = hi;
-      if (LO) *reinterpret_cast<uint4*>(dst_lo + doff + i * KPI * 128) = lo;
+  for (int i = 0; i < Gm::NH; ++i) {
+    const int pid = i < Gm::NH / 2 ? pa : pb;
+    const int row = key0 + i * Gm::KPI - (i < Gm::NH / 2 ? 0 : kPage);  // row within the page
+    const bool ok = pid >= 0 && key0 + i * Gm::KPI < valid;
+    const int64_t prow = ((int64_t)(ok ? pid : 0) * hkv + g) * kPage + row;
+    // predicated loads: nothing here waits for the data (it is used a half later)
+    if (F == MIXATTN_KV_F16) {
+      r.q[i] = ldg_u128_pred(q_plane + prow * Gm::RB + src_col, ok);
+    } else {
+      const uint2 x = ldg_u64_pred(q_plane + prow * Gm::RB + src_col, ok);
+      r.q[i].x = x.x;
+      r.q[i].y = x.y;
+      r.s[i] = ldg_u16_pred(s_plane + prow * Gm::NB + b, ok);
     }
   }
 }
 
-// One out-of-line copy per format serves both key halves and both operands: the
-// dequant code of the K and V groups then shares instruction-cache lines.  The
-// fp16 "dequantisation" (a swizzled copy) stays inline.
+// Convert the raw bytes of key half h (loaded by load_half) into the swizzled
+// fp16 operand tile: hi, and the exact lo for quantised formats.
 template <int F, int D, bool LO>
-__device__ __noinline__ void dequant_half_call(const uint8_t* __restrict__ raw_q, const uint8_t* __restrict__ raw_s,
-                                               uint8_t* __restrict__ dst_hi, uint8_t* __restrict__ dst_lo,
-                                               int valid_keys, int t0, int H) {
-  dequant_half_body<F, D, LO>(raw_q, raw_s, dst_hi, dst_lo, valid_keys, t0, H);
+__device__ __forceinline__ void convert_half(const HalfRaw<F, D>& r, uint8_t* __restrict__ dst_hi,
+                                             uint8_t* __restrict__ dst_lo, int h, int t0) {
+  using Gm = DequantGeom<F, D>;
+  const int dc = t0 % Gm::CPR, key0 = t0 / Gm::CPR;
+  const int half = dc >> 3, cc = dc & 7;
+  const int shift = F == MIXATTN_KV_Q4_0 ? ((dc >> 1) & 1) * 4 : 0;  // low nibbles, then high nibbles
+  const int kh = key0 + kChunkN / 2 * h;
+  const uint32_t doff = (uint32_t)(half * (kChunkN * 128) + kh * 128 + ((cc ^ (key0 & 7)) << 4));
+#pragma unroll
+  for (int i = 0; i < Gm::NH; ++i) {
+    uint4 hi, lo = make_uint4(0u, 0u, 0u, 0u);
+    if (F == MIXATTN_KV_F16) {
+      hi = r.q[i];
+    } else {
+      const uint32_t sc = prmt(r.s[i], 0u, 0x1010u);  // the scale in both halves
+      uint32_t h0, h1, h2, h3;
+      if (F == MIXATTN_KV_Q8_0) {
+        s8x4_to_f16x2x2(r.q[i].x, h0, h1);
+        s8x4_to_f16x2x2(r.q[i].y, h2, h3);
+      } else {
+        u4x4_to_f16x2x2((r.q[i].x >> shift) & 0x0F0F0F0Fu, h0, h1);
+        u4x4_to_f16x2x2((r.q[i].y >> shift) & 0x0F0F0F0Fu, h2, h3);
+      }
+      split_hilo(h0, sc, hi.x, lo.x);
+      split_hilo(h1, sc, hi.y, lo.y);
+      split_hilo(h2, sc, hi.z, lo.z);
+      split_hilo(h3, sc, hi.w, lo.w);
+    }
+    *reinterpret_cast<uint4*>(dst_hi + doff + i * Gm::KPI * 128) = hi;
+    if (LO) *reinterpret_cast<uint4*>(dst_lo + doff + i * Gm::KPI * 128) = lo;
+  }
 }
 
+// The whole loop of one dequant group over the KV tiles of a chunk tile (one
+// out-of-line copy per format serves the K and the V group, which then share
+// instruction-cache lines).
+//   K group: K(j) goes to buffer j % 2 (hi at dst_hi[j%2], lo at dst_lo[j%2])
+//     once QK(j-2) has released it (qk_done[j%2]); after both halves it arrives
+//     on ready[j%2].
+//   V group: V(j) goes to the single buffer, half h once the PV MMAs of tile
+//     j-1 that read that half are done (pvh_done[h]); it arrives on ready[h]
+//     after each half.
+// Returns false when the group left early (a timeout here or elsewhere).
 template <int F, int D, bool LO>
-__device__ __forceinline__ void dequant_half(const uint8_t* raw_q, const uint8_t* raw_s, uint8_t* dst_hi,
-                                             uint8_t* dst_lo, int valid_keys, int t0, int H) {
-  if constexpr (F == MIXATTN_KV_F16)
-    dequant_half_body<F, D, LO>(raw_q, raw_s, dst_hi, dst_lo, valid_keys, t0, H);
-  else
-    dequant_half_call<F, D, LO>(raw_q, raw_s, dst_hi, dst_lo, valid_keys, t0, H);
+__device__ __noinline__ bool dequant_loop(const uint8_t* __restrict__ q_plane, const uint16_t* __restrict__ s_plane,
+                                          const int32_t* __restrict__ pt_row, int n_pages_row, int num_pages,
+                                          int hkv, int g, int key_end, int n_kv, int t0, bool is_k,
+                                          uint8_t* dst_hi0, uint8_t* dst_lo0, uint8_t* dst_hi1, uint8_t* dst_lo1,
+                                          uint64_t* free_bars, uint64_t* ready, int bar_id,
+                                          volatile int* abort_flag, unsigned int* err) {
+  bool ok = true;
+  // page ids of key half (j, h); the bounds check happens at load time
+  auto pid_of = [&](int pg) { return ldg_s32_or(pt_row + pg, pg < n_pages_row && pg * kPage < key_end, kNoPage); };
+  auto valid_of = [&](int j, int h) { return key_end - j * kChunkN - h * (kChunkN / 2); };
+  // one half: wait until its destination is free, convert, publish
+  auto process = [&](const HalfRaw<F, D>& r, int j, int h) -> bool {
+    if (is_k) {
+      if (h == 0 && j > 1) ok = mbar_wait(&free_bars[j & 1], (uint32_t)(((j - 2) >> 1) & 1), err) && ok;
+    } else {
+      if (j > 0) ok = mbar_wait(&free_bars[h], (uint32_t)((j - 1) & 1), err) && ok;
+    }
+    tc_fence_after();
+    const bool b1 = is_k && (j & 1);
+    convert_half<F, D, LO>(r, b1 ? dst_hi1 : dst_hi0, b1 ? dst_lo1 : dst_lo0, h, t0);
+    fence_proxy_async_smem();
+    if (bar_any(bar_id, 128, !ok || *abort_flag)) {  // one decision for the group
+      *abort_flag = 1;
+      return false;
+    }
+    if (t0 == 0) {
+      if (!is_k) mbar_arrive(&ready[h]);
+      else if (h == 1) mbar_arrive(&ready[j & 1]);
+    }
+    return true;
+  };
+  HalfRaw<F, D> ra, rb;
+  int pa = pid_of(0), pb = pid_of(1);
+  load_half<F, D>(ra, q_plane, s_plane, pa, pb, num_pages, hkv, g, valid_of(0, 0), t0, err);
+  pa = pid_of(2);
+  pb = pid_of(3);
+  for (int j = 0; j < n_kv; ++j) {
+    // half 0 of tile j is in ra; fetch half 1 into rb meanwhile
+    load_half<F, D>(rb, q_plane, s_plane, pa, pb, num_pages, hkv, g, valid_of(j, 1), t0, err);
+    pa = pid_of(4 * (j + 1));
+    pb = pid_of(4 * (j + 1) + 1);
+    if (!process(ra, j, 0)) return false;
+    // half 1 is in rb; fetch half 0 of tile j+1 into ra meanwhile
+    if (j + 1 < n_kv) load_half<F, D>(ra, q_plane, s_plane, pa, pb, num_pages, hkv, g, valid_of(j + 1, 0), t0, err);
+    pa = pid_of(4 * (j + 1) + 2);
+    pb = pid_of(4 * (j + 1) + 3);
+    if (!process(rb, j, 1)) return false;
+  }
+  return ok;
 }
 
 // Chunk tile: 128 rows (128/G query tokens x G heads of kv head `t.kvh`) against
-// the keys they can see, in 128-key KV tiles j.  Each K and V operand tile is
-// handled as two 64-key halves, so the dequantisation of tile j+1 overlaps the
-// MMAs of tile j half by half.  Roles:
-//   K producer (warp 13, one thread) and V producer (warp 14, one thread): bulk
-//     copies of the raw K (V) pages of tile j into a ring of raw stages, each
-//     stage refilled once its dequant group is done with it; the page ids are
-//     fetched one tile ahead;
-//   K group (warps 4-7): dequantises the upper, then the lower key half of K(j),
-//     each once QK of tile j-1 has released that half;
-//   V group (warps 8-11): the same for V(j) against the two halves of PV(j-1);
+// the keys they can see, in 128-key KV tiles j.  Roles:
+//   K group (warps 4-7): loads the raw K bytes of tile j straight from the cache
+//     planes (one 64-key half ahead of their use) and dequantises K(j) into
+//     operand buffer j%2 once QK(j-2) has released it;
+//   V group (warps 8-11): the same for V(j), into a single buffer, key half h
+//     once the PV MMAs of tile j-1 that read that half are done;
 //   softmax group (warps 0-3, thread i = TMEM lane i = query row i): reads
 //     S[j%2] twice (row max, then P = 2^(s - m) as fp16 written over the
 //     scores), waits for PV(j-1), rescales O when the row max moved;
-//   MMA warp (warp 12, one thread): issues QK(j) into S[j%2] (upper key half
-//     first: P(j-2) lives in the lower 64 columns until PV(j-2) has read it),
-//     then PV(j-1), each half as soon as its operand half is ready.
-// TMEM: Q (A operand, fp16) | S0 | S1 | O (fp32).  Every wait is bounded; a
-// timeout in any role makes all of them leave their loops.
+//   MMA warp (warp 12, one thread): issues QK(j) into S[j%2] once K(j) is
+//     written and PV(j-2) has read the P that tile j-2 left there, then PV(j-1),
+//     each key half as soon as its V half is written.
+// The MMA issue blocks its thread for about the MMA's duration, which is why
+// one warp does nothing else.  TMEM: Q (A operand, fp16) | S0 | S1 | O (fp32).
+// Every wait is bounded; a timeout in any role makes all of them leave their
+// loops.
 template <int FK, int FV, int D>
 __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& t, uint8_t* smem_raw,
                                            unsigned int* err) {
   using L = ChunkSmem<FK, FV, D>;
-  constexpr int NKS = L::kKStages, NVS = L::kVStages;
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kQCol = 0, kSCol0 = 128, kSCol1 = 256, kOCol = 384;
   constexpr int kGroup = 128;          // threads per warp group
-  constexpr int kHalfN = kChunkN / 2;  // keys per operand half
   constexpr int kBarSoftmax = 1, kBarK = 2, kBarV = 3;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint64_t* k_full = bars;                 // [NKS] raw K stage landed
-  uint64_t* k_free = k_full + NKS;         // [NKS] raw K stage consumed
-  uint64_t* v_full = k_free + NKS;         // [NVS]
-  uint64_t* v_free = v_full + NVS;         // [NVS]
-  uint64_t* kdeq = v_free + NVS;           // [2] K half h of the current tile written
-  uint64_t* vdeq = kdeq + 2;               // [2] V half h written
-  uint64_t* qkh_done = vdeq + 2;           // [2] the QK MMAs reading K half h are done
-  uint64_t* pvh_done = qkh_done + 2;       // [2] the PV MMAs reading V half h are done
-  uint64_t* qk_done = pvh_done + 2;        // [2] S[st] holds the scores of the tile
+  uint64_t* kdeq = bars;                   // [2] K(j) written to buffer j%2
+  uint64_t* vdeq = kdeq + 2;               // [2] V half h of the current tile written
+  uint64_t* pvh_done = vdeq + 2;           // [2] the PV MMAs reading V half h are done
+  uint64_t* qk_done = pvh_done + 2;        // [2] S[st] holds the scores of the tile; K buffer st free
   uint64_t* pv_done = qk_done + 2;         // [2] PV of the tile done (P in S[st] read)
   uint64_t* sm_done = pv_done + 2;         // [2] P of the tile written, O rescaled
   uint64_t* mma_fin = sm_done + 2;         // [1] every MMA of the tile done
-  constexpr int kNumBars = 2 * NKS + 2 * NVS + 15;
+  constexpr int kNumBars = 13;
   static_assert(kNumBars * 8 + 8 <= L::kBarBytes, "barrier area too small");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kNumBars) + 1;
@@ -738,77 +778,25 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
   __syncthreads();
   tc_fence_after();
 
-  constexpr uint32_t kIdescQK = idesc_f16_f32(128, kHalfN, false, false);
+  constexpr uint32_t kIdescQK = idesc_f16_f32(128, kChunkN, false, false);
   constexpr uint32_t kIdescPV = idesc_f16_f32(128, D, false, true);
-  const uint32_t sKh = smem_u32(smem + L::kKh), sKl = smem_u32(smem + L::kKl);
+  const uint32_t sK0 = smem_u32(smem + L::kK0), sK1 = smem_u32(smem + L::kK1);
   const uint32_t sVh = smem_u32(smem + L::kVh), sVl = smem_u32(smem + L::kVl);
   bool ok = true;
   float m_run = -CUDART_INF_F, l_run = 0.f;
 
-  if (tid >= kGroup && tid < 2 * kGroup) {
-    // ======================= K group (warps 4-7) =======================
-    const int dt = tid - kGroup;
-    for (int j = 0; j < n_kv; ++j) {
-      const int rs = j % NKS;
-      const uint32_t ph_prev = (uint32_t)((j - 1) & 1);
-      ok = mbar_wait(&k_full[rs], (uint32_t)((j / NKS) & 1), err) && ok;
-      const uint8_t* raw = smem + L::kKRaw + rs * L::kKRawBytes;
-      const int valid_keys = key_end - j * kChunkN;
-      // the upper key half first: the MMA warp issues its QK half first
-      if (j > 0) ok = mbar_wait(&qkh_done[1], ph_prev, err) && ok;
-      tc_fence_after();
-      dequant_half<FK, D, L::kKLo>(raw, raw + L::kKsOff, smem + L::kKh, smem + L::kKl, valid_keys, dt, 1);
-      fence_proxy_async_smem();
-      if (bar_any(kBarK, kGroup, !ok || *abort_flag)) {  // one decision for the group
-        *abort_flag = 1;
-        break;
-      }
-      if (dt == 0) mbar_arrive(&kdeq[1]);
-      if (j > 0) ok = mbar_wait(&qkh_done[0], ph_prev, err) && ok;
-      tc_fence_after();
-      dequant_half<FK, D, L::kKLo>(raw, raw + L::kKsOff, smem + L::kKh, smem + L::kKl, valid_keys, dt, 0);
-      fence_proxy_async_smem();
-      if (bar_any(kBarK, kGroup, !ok || *abort_flag)) {
-        *abort_flag = 1;
-        break;
-      }
-      if (dt == 0) {
-        mbar_arrive(&kdeq[0]);
-        mbar_arrive(&k_free[rs]);  // the raw K stage may be refilled
-      }
-    }
-  } else if (tid >= 2 * kGroup && tid < 3 * kGroup) {
-    // ======================= V group (warps 8-11) =======================
-    const int dt = tid - 2 * kGroup;
-    for (int j = 0; j < n_kv; ++j) {
-      const int rs = j % NVS;
-      const uint32_t ph_prev = (uint32_t)((j - 1) & 1);
-      ok = mbar_wait(&v_full[rs], (uint32_t)((j / NVS) & 1), err) && ok;
-      const uint8_t* raw = smem + L::kVRaw + rs * L::kVRawBytes;
-      const int valid_keys = key_end - j * kChunkN;
-      // the lower key half first: PV reads it first
-      if (j > 0) ok = mbar_wait(&pvh_done[0], ph_prev, err) && ok;
-      tc_fence_after();
-      dequant_half<FV, D, L::kVLo>(raw, raw + L::kVsOff, smem + L::kVh, smem + L::kVl, valid_keys, dt, 0);
-      fence_proxy_async_smem();
-      if (bar_any(kBarV, kGroup, !ok || *abort_flag)) {
-        *abort_flag = 1;
-        break;
-      }
-      if (dt == 0) mbar_arrive(&vdeq[0]);
-      if (j > 0) ok = mbar_wait(&pvh_done[1], ph_prev, err) && ok;
-      tc_fence_after();
-      dequant_half<FV, D, L::kVLo>(raw, raw + L::kVsOff, smem + L::kVh, smem + L::kVl, valid_keys, dt, 1);
-      fence_proxy_async_smem();
-      if (bar_any(kBarV, kGroup, !ok || *abort_flag)) {
-        *abort_flag = 1;
-        break;
-      }
-      if (dt == 0) {
-        mbar_arrive(&vdeq[1]);
-        mbar_arrive(&v_free[rs]);
-      }
-    }
+  if (tid >= kGroup && tid < 3 * kGroup) {
+    // =========== K group (warps 4-7) and V group (warps 8-11): dequantisation ===========
+    const bool is_k = tid < 2 * kGroup;
+    const bool done_ok =
+        is_k ? dequant_loop<FK, D, L::kKLo>(p.k_quant, p.k_scale, pt_row, n_pages_row, p.num_pages, p.hkv, g, key_end,
+                                            n_kv, tid - kGroup, true, smem + L::kK0, smem + L::kK0 + L::kTile,
+                                            smem + L::kK1, smem + L::kK1 + L::kTile, qk_done, kdeq, kBarK,
+                                            abort_flag, err)
+             : dequant_loop<FV, D, L::kVLo>(p.v_quant, p.v_scale, pt_row, n_pages_row, p.num_pages, p.hkv, g, key_end,
+                                            n_kv, tid - 2 * kGroup, false, smem + L::kVh, smem + L::kVl, smem + L::kVh,
+                                            smem + L::kVl, pvh_done, vdeq, kBarV, abort_flag, err);
+    if (!done_ok) *abort_flag = 1;
   } else if (tid < kGroup) {
     // ======================= softmax group =======================
     const float sl2 = p.scale_log2;
@@ -926,22 +914,18 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
       if (j < n_kv) {
         const int st = j & 1;
         const uint32_t s_col = tmem + (st ? kSCol1 : kSCol0);
-#pragma unroll
-        for (int hf = 1; hf >= 0; --hf) {
-          ok = mbar_wait(&kdeq[hf], (uint32_t)(j & 1), err) && ok;  // K half hf of tile j written
-          // the lower 64 columns of S[st] hold P(j-2) until PV(j-2) has read it
-          if (hf == 0 && j > 1) ok = mbar_wait(&pv_done[st], (uint32_t)(((j - 2) >> 1) & 1), err) && ok;
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (uint32_t)((ks >> 2) * (kChunkN * 128) + (ks & 3) * 32 + hf * (kHalfN * 128));
-            tc_mma_ts(s_col + hf * kHalfN, tmem + kQCol + 8 * ks, sw128_desc(sKh + off, 16, 1024), kIdescQK,
-                      ks > 0 ? 1u : 0u);
-            if (L::kKLo)
-              tc_mma_ts(s_col + hf * kHalfN, tmem + kQCol + 8 * ks, sw128_desc(sKl + off, 16, 1024), kIdescQK, 1u);
-          }
-          tc_commit(&qkh_done[hf]);
+        ok = mbar_wait(&kdeq[st], (uint32_t)((j >> 1) & 1), err) && ok;  // K(j) written to buffer st
+        // S[st] holds P(j-2) until PV(j-2) has read it
+        if (j > 1) ok = mbar_wait(&pv_done[st], (uint32_t)(((j - 2) >> 1) & 1), err) && ok;
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t kh = st ? sK1 : sK0;
+#pragma unroll 1
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (uint32_t)((ks >> 2) * (kChunkN * 128) + (ks & 3) * 32);
+          tc_mma_ts(s_col, tmem + kQCol + 8 * ks, sw128_desc(kh + off, 16, 1024), kIdescQK, ks > 0 ? 1u : 0u);
+          if (L::kKLo)
+            tc_mma_ts(s_col, tmem + kQCol + 8 * ks, sw128_desc(kh + L::kTile + off, 16, 1024), kIdescQK, 1u);
         }
         if (!ok) break;
         tc_commit(&qk_done[st]);
@@ -974,69 +958,6 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
     // nothing this thread started may still run when TMEM is released
     tc_commit(mma_fin);
     mbar_wait(mma_fin, 0u, err);
-  } else if (tid == 3 * kGroup + 32 || tid == 3 * kGroup + 64) {
-    // ===== producers (warps 13 and 14, one thread each): raw K / raw V pages of tile j =====
-    const bool is_k = tid == 3 * kGroup + 32;
-    const int ns = is_k ? NKS : NVS;
-    uint64_t* full = is_k ? k_full : v_full;
-    uint64_t* free_ = is_k ? k_free : v_free;
-    uint8_t* ring = smem + (is_k ? L::kKRaw : L::kVRaw);
-    const int stage_bytes = is_k ? L::kKRawBytes : L::kVRawBytes;
-    const int q_page = is_k ? L::kKqPage : L::kVqPage, s_page = is_k ? L::kKsPage : L::kVsPage;
-    const int s_off = is_k ? L::kKsOff : L::kVsOff;
-    const uint8_t* q_src = is_k ? p.k_quant : p.v_quant;
-    const uint8_t* s_src = reinterpret_cast<const uint8_t*>(is_k ? p.k_scale : p.v_scale);
-    int pids[L::kPagesPerTile];
-    // page ids of tile jj (validated; -1 = no page: keys past the tile's end)
-    auto load_pids = [&](int jj) {
-#pragma unroll
-      for (int pj = 0; pj < L::kPagesPerTile; ++pj) {
-        const int pg = jj * L::kPagesPerTile + pj;
-        int pid = -1;
-        if (pg < n_pages_row && pg * kPage < key_end) {
-          pid = pt_row[pg];
-          if (pid < 0 || pid >= p.num_pages) {
-            set_device_error(err, MIXATTN_DEVERR_PAGE_ID);
-            pid = -1;
-          }
-        }
-        pids[pj] = pid;
-      }
-    };
-    auto issue = [&](int s) {
-      uint8_t* raw = ring + s * stage_bytes;
-      uint32_t bytes = 0;
-#pragma unroll
-      for (int pj = 0; pj < L::kPagesPerTile; ++pj)
-        if (pids[pj] >= 0) bytes += q_page + s_page;
-      mbar_arrive_expect_tx(&full[s], bytes);
-#pragma unroll
-      for (int pj = 0; pj < L::kPagesPerTile; ++pj) {
-        if (pids[pj] < 0) continue;
-        const int64_t prow = ((int64_t)pids[pj] * p.hkv + g) * kPage;  // first plane row of (page, head)
-        bulk_g2s(raw + pj * q_page, q_src + prow * (q_page / kPage), q_page, &full[s]);
-        if (s_page) bulk_g2s(raw + s_off + pj * s_page, s_src + prow * (s_page / kPage), s_page, &full[s]);
-      }
-    };
-    int issued = 0;
-    for (; issued < ns && issued < n_kv; ++issued) {
-      load_pids(issued);
-      issue(issued);
-    }
-    if (issued < n_kv) load_pids(issued);  // one tile ahead
-    for (int j = 0; issued < n_kv; ++j) {
-      // stage j%ns is free once its dequant group is done with tile j
-      const int rs = j % ns;
-      ok = mbar_wait(&free_[rs], (uint32_t)((j / ns) & 1), err) && ok;
-      if (!ok || *abort_flag) break;
-      issue(rs);
-      ++issued;
-      if (issued < n_kv) load_pids(issued);
-    }
-    if (!ok) *abort_flag = 1;
-    // no copy this thread started may still land when the stages are released
-    for (int jj = max(0, issued - ns); jj < issued; ++jj)
-      mbar_wait(&full[jj % ns], (uint32_t)((jj / ns) & 1), err);
   }
   tc_fence_before();
   __syncthreads();

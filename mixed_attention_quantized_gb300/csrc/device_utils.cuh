@@ -123,6 +123,45 @@ __device__ __forceinline__ uint2 ldg_u64(const void* p) {
   asm volatile("ld.global.nc.L1::no_allocate.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
 }
+// Predicated loads: zeros when `pred` is false (the address is then not used).
+// One asm statement each, so no select on the loaded value stalls the issuing
+// thread before the data is needed.
+__device__ __forceinline__ uint2 ldg_u64_pred(const void* p, bool pred) {
+  uint2 v;
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.b32 q, %3, 0;\n mov.b32 %0, 0;\n mov.b32 %1, 0;\n"
+      " @q ld.global.nc.L1::no_allocate.v2.b32 {%0,%1}, [%2];\n}"
+      : "=r"(v.x), "=r"(v.y)
+      : "l"(p), "r"((uint32_t)pred));
+  return v;
+}
+__device__ __forceinline__ uint4 ldg_u128_pred(const void* p, bool pred) {
+  uint4 v;
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.b32 q, %5, 0;\n mov.b32 %0, 0;\n mov.b32 %1, 0;\n mov.b32 %2, 0;\n"
+      " mov.b32 %3, 0;\n @q ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];\n}"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p), "r"((uint32_t)pred));
+  return v;
+}
+__device__ __forceinline__ int ldg_s32_or(const void* p, bool pred, int dflt) {
+  int v;
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n mov.b32 %0, %3;\n"
+      " @q ld.global.nc.b32 %0, [%1];\n}"
+      : "=r"(v)
+      : "l"(p), "r"((uint32_t)pred), "r"(dflt));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_u16_pred(const void* p, bool pred) {
+  uint32_t v;
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n mov.b32 %0, 0;\n"
+      " @q ld.global.nc.u16 %0, [%1];\n}"
+      : "=r"(v)
+      : "l"(p), "r"((uint32_t)pred));
+  return v;
+}
 __device__ __forceinline__ uint4 ldg_u128(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
