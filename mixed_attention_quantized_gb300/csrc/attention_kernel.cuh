@@ -780,8 +780,13 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
 
   constexpr uint32_t kIdescQK = idesc_f16_f32(128, kChunkN, false, false);
   constexpr uint32_t kIdescPV = idesc_f16_f32(128, D, false, true);
-  const uint32_t sK0 = smem_u32(smem + L::kK0), sK1 = smem_u32(smem + L::kK1);
-  const uint32_t sVh = smem_u32(smem + L::kVh), sVl = smem_u32(smem + L::kVl);
+  // operand descriptors, split into words: K tiles K-major (SBO 1024 B between
+  // 8-key groups), V tiles MN-major (LBO = one 64-column slab, 128 keys x 128 B)
+  const uint32_t dK0 = (uint32_t)sw128_desc(smem_u32(smem + L::kK0), 16, 1024);
+  const uint32_t dK1 = (uint32_t)sw128_desc(smem_u32(smem + L::kK1), 16, 1024);
+  const uint32_t dHiK = (uint32_t)(sw128_desc(0, 16, 1024) >> 32);
+  const uint32_t dV = (uint32_t)sw128_desc(smem_u32(smem + L::kVh), kChunkN * 128, 1024);
+  const uint32_t dHiV = (uint32_t)(sw128_desc(0, kChunkN * 128, 1024) >> 32);
   bool ok = true;
   float m_run = -CUDART_INF_F, l_run = 0.f;
 
@@ -919,13 +924,13 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
         if (j > 1) ok = mbar_wait(&pv_done[st], (uint32_t)(((j - 2) >> 1) & 1), err) && ok;
         if (!ok) break;
         tc_fence_after();
-        const uint32_t kh = st ? sK1 : sK0;
-#pragma unroll 1
+        const uint32_t kd = st ? dK1 : dK0;  // low descriptor word of K buffer st
+#pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (uint32_t)((ks >> 2) * (kChunkN * 128) + (ks & 3) * 32);
-          tc_mma_ts(s_col, tmem + kQCol + 8 * ks, sw128_desc(kh + off, 16, 1024), kIdescQK, ks > 0 ? 1u : 0u);
-          if (L::kKLo)
-            tc_mma_ts(s_col, tmem + kQCol + 8 * ks, sw128_desc(kh + L::kTile + off, 16, 1024), kIdescQK, 1u);
+          const uint32_t off = (uint32_t)((ks >> 2) * (kChunkN * 128) + (ks & 3) * 32) >> 4;
+          if (ks == 0) tc_mma_ts_w<0>(s_col, tmem + kQCol, kd + off, dHiK, kIdescQK);
+          else tc_mma_ts_w<1>(s_col, tmem + kQCol + 8 * ks, kd + off, dHiK, kIdescQK);
+          if (L::kKLo) tc_mma_ts_w<1>(s_col, tmem + kQCol + 8 * ks, kd + (L::kTile >> 4) + off, dHiK, kIdescQK);
         }
         if (!ok) break;
         tc_commit(&qk_done[st]);
@@ -942,10 +947,10 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
 #pragma unroll
           for (int kk = 4 * hv; kk < 4 * hv + 4; ++kk) {
             const uint32_t pa = p_col + 8 * kk;  // P columns of keys 16kk..16kk+15
-            const uint32_t boff = (uint32_t)(kk * 16 * 128);
-            const uint32_t acc = (jp > 0 || kk > 0) ? 1u : 0u;
-            tc_mma_ts(tmem + kOCol, pa, sw128_desc(sVh + boff, kChunkN * 128, 1024), kIdescPV, acc);
-            if (L::kVLo) tc_mma_ts(tmem + kOCol, pa, sw128_desc(sVl + boff, kChunkN * 128, 1024), kIdescPV, 1u);
+            const uint32_t boff = (uint32_t)(kk * 16 * 128) >> 4;
+            if (kk == 0) tc_mma_ts_w(tmem + kOCol, pa, dV + boff, dHiV, kIdescPV, jp > 0 ? 1u : 0u);
+            else tc_mma_ts_w<1>(tmem + kOCol, pa, dV + boff, dHiV, kIdescPV);
+            if (L::kVLo) tc_mma_ts_w<1>(tmem + kOCol, pa, dV + (L::kTile >> 4) + boff, dHiV, kIdescPV);
           }
           tc_commit(&pvh_done[hv]);
         }
