@@ -567,20 +567,26 @@ __device__ __forceinline__ void load_half(HalfRaw<F, D>& r, const uint8_t* __res
     if (bad_a) pa = kNoPage;
     if (bad_b) pb = kNoPage;
   }
+  // first plane row of this thread's keys in each page; key i then sits a
+  // compile-time number of rows further
+  const int64_t row_a = ((int64_t)(pa >= 0 ? pa : 0) * hkv + g) * kPage + key0;
+  const int64_t row_b = ((int64_t)(pb >= 0 ? pb : 0) * hkv + g) * kPage + key0 - kPage;
+  const uint8_t* qa = q_plane + row_a * Gm::RB + src_col;
+  const uint8_t* qb = q_plane + row_b * Gm::RB + src_col;
+  const uint16_t* sa = s_plane + row_a * Gm::NB + b;
+  const uint16_t* sb = s_plane + row_b * Gm::NB + b;
 #pragma unroll
   for (int i = 0; i < Gm::NH; ++i) {
-    const int pid = i < Gm::NH / 2 ? pa : pb;
-    const int row = key0 + i * Gm::KPI - (i < Gm::NH / 2 ? 0 : kPage);  // row within the page
-    const bool ok = pid >= 0 && key0 + i * Gm::KPI < valid;
-    const int64_t prow = ((int64_t)(ok ? pid : 0) * hkv + g) * kPage + row;
+    const bool first = i < Gm::NH / 2;
+    const bool ok = (first ? pa : pb) >= 0 && key0 + i * Gm::KPI < valid;
     // predicated loads: nothing here waits for the data (it is used a half later)
     if (F == MIXATTN_KV_F16) {
-      r.q[i] = ldg_u128_pred(q_plane + prow * Gm::RB + src_col, ok);
+      r.q[i] = ldg_u128_pred((first ? qa : qb) + i * Gm::KPI * Gm::RB, ok);
     } else {
-      const uint2 x = ldg_u64_pred(q_plane + prow * Gm::RB + src_col, ok);
+      const uint2 x = ldg_u64_pred((first ? qa : qb) + i * Gm::KPI * Gm::RB, ok);
       r.q[i].x = x.x;
       r.q[i].y = x.y;
-      r.s[i] = ldg_u16_pred(s_plane + prow * Gm::NB + b, ok);
+      r.s[i] = ldg_u16_pred((first ? sa : sb) + i * Gm::KPI * Gm::NB, ok);
     }
   }
 }
@@ -829,9 +835,9 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
             if (kbase + 32 * c + e > pos) a[e] = ninf;
         }
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          mx0 = fmaxf(mx0, __uint_as_float(a[e]));
-          mx1 = fmaxf(mx1, __uint_as_float(a[e + 1]));
+        for (int e = 0; e < 32; e += 4) {
+          mx0 = fmax3(mx0, __uint_as_float(a[e]), __uint_as_float(a[e + 1]));
+          mx1 = fmax3(mx1, __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
         }
       }
       // running max in log2 units (the score scale is positive, so it commutes with max)
@@ -839,8 +845,10 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
       const float alpha = ex2(m_run - m_new);
       const float neg_m = -m_new;
       // pass 2: P = 2^(s*scale - m) as fp16 over the consumed scores (chunk c of
-      // P lands on columns of chunks already read); row sums in fp32
-      float sum0 = 0.f, sum1 = 0.f;
+      // P lands on columns of chunks already read); row sums in fp32.  The
+      // scale-and-shift and the sums run on fp32 pairs.
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(neg_m, neg_m);
+      uint64_t sum_a = f2_pack(0.f, 0.f), sum_b = sum_a;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         tmem_ld32(s_col + 32 * c, a);
@@ -853,17 +861,22 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const float a0 = ex2(fmaf(__uint_as_float(a[e]), sl2, neg_m));
-          const float a1 = ex2(fmaf(__uint_as_float(a[e + 1]), sl2, neg_m));
-          const float a2 = ex2(fmaf(__uint_as_float(a[e + 2]), sl2, neg_m));
-          const float a3 = ex2(fmaf(__uint_as_float(a[e + 3]), sl2, neg_m));
-          sum0 += a0 + a1;
-          sum1 += a2 + a3;
-          pk[e >> 1] = pack_f16x2(a0, a1);
-          pk[(e >> 1) + 1] = pack_f16x2(a2, a3);
+          float x0, x1, x2, x3;
+          f2_unpack(ffma2(f2_pack(__uint_as_float(a[e]), __uint_as_float(a[e + 1])), sl2x2, negm2), x0, x1);
+          f2_unpack(ffma2(f2_pack(__uint_as_float(a[e + 2]), __uint_as_float(a[e + 3])), sl2x2, negm2), x2, x3);
+          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+          sum_a = fadd2(sum_a, f2_pack(p0, p1));
+          sum_b = fadd2(sum_b, f2_pack(p2, p3));
+          pk[e >> 1] = pack_f16x2(p0, p1);
+          pk[(e >> 1) + 1] = pack_f16x2(p2, p3);
         }
         tmem_st16(s_col + 16 * c, pk);
       }
+      float sum0, sum1, sum2, sum3;
+      f2_unpack(sum_a, sum0, sum1);
+      f2_unpack(sum_b, sum2, sum3);
+      sum0 += sum2;
+      sum1 += sum3;
       l_run = l_run * alpha + (sum0 + sum1);
       m_run = m_new;
       // the running O may be rescaled only once PV(j-1) has finished with it
@@ -875,8 +888,14 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
           for (int ch = 0; ch < D / 32; ++ch) {
             tmem_ld32(tmem + lane_base + kOCol + 32 * ch, a);
             tmem_wait_ld();
+            const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) a[e] = __float_as_uint(__uint_as_float(a[e]) * alpha);
+            for (int e = 0; e < 32; e += 2) {
+              float y0, y1;
+              f2_unpack(fmul2(f2_pack(__uint_as_float(a[e]), __uint_as_float(a[e + 1])), al2), y0, y1);
+              a[e] = __float_as_uint(y0);
+              a[e + 1] = __float_as_uint(y1);
+            }
             tmem_st32(tmem + lane_base + kOCol + 32 * ch, a);
           }
         }
