@@ -133,20 +133,23 @@ __device__ __forceinline__ void load_scales(const uint8_t* p, float (&out)[NB]) 
   }
 }
 
-// Barrier over the 8 warps of a decode tile (a fused-launch CTA has more warps,
-// which leave before the tile starts).
-__device__ __forceinline__ void decode_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+// Barrier over the 8 warps of a decode tile (a fused-launch CTA runs one tile
+// on each half of its 16 warps, each half on its own named barrier).
+__device__ __forceinline__ void decode_sync(int half) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + half), "n"(kThreads) : "memory");
+}
 
 template <int FK, int FV, int D, int NS>
 __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc& t, int dec_idx, uint8_t* smem,
-                                            unsigned int* err) {
+                                            unsigned int* err, int half) {
   using S = DecodeSmem<FK, FV, D>;
   constexpr int NB = D / kBlock;   // scale blocks per row
   constexpr int KS = D / 16;       // k-steps of QK / M-tiles of PV
   constexpr int RBK = row_bytes<FK, D>();
   constexpr int RBV = row_bytes<FV, D>();
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // `half`: which 8 warps of the CTA run this tile (a fused-launch CTA runs two)
+  const int tid = threadIdx.x - half * kThreads, warp = tid >> 5, lane = tid & 31;
   const int r = lane >> 2, c = lane & 3;
   const int G = p.group;
   const int g = t.kvh;
@@ -416,7 +419,7 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   // ---------------- warp partial -> shared memory ----------------
   l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 1);
   l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 2);
-  decode_sync();  // the staging rings are no longer needed: reuse them as merge scratch
+  decode_sync(half);  // the staging rings are no longer needed: reuse them as merge scratch
   float* ws = reinterpret_cast<float*>(smem);
   float* wm = ws + warp * S::kPerWarp;  // m[8], l[8], O[8][D]
   const int h0 = 2 * c, h1 = 2 * c + 1;
@@ -436,7 +439,7 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
       wm[16 + h1 * D + d_hi] = o_acc[tt][3];
     }
   }
-  decode_sync();
+  decode_sync(half);
 
   // ---------------- merge the 8 warps ----------------
   const int n_out = G * D;
@@ -469,13 +472,14 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
 
   // ---------------- last CTA of (row, kv head) merges the splits ----------------
   __threadfence();
-  decode_sync();
-  __shared__ int s_last;
+  decode_sync(half);
+  __shared__ int s_last_of[2];
+  int& s_last = s_last_of[half];
   if (tid == 0) {
     const unsigned prev = atomicAdd(&p.counters[(int64_t)t.row * p.hkv + g], 1u);
     s_last = (prev == (unsigned)(ri.n_splits - 1));
   }
-  decode_sync();
+  decode_sync(half);
   if (!s_last) return;
   __threadfence();
   const int first = dec_idx - split;
@@ -995,9 +999,17 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
 // memory for the chunk role).
 template <int FK, int FV, int D>
 struct FusedSmem {
-  static constexpr int kDec2 = DecodeSmem<FK, FV, D>::total(2);
-  static constexpr int kBytes = ChunkSmem<FK, FV, D>::kTotal > kDec2 ? ChunkSmem<FK, FV, D>::kTotal : kDec2;
-  static constexpr int kDecodeStages = DecodeSmem<FK, FV, D>::stages_for(kBytes - 16);
+  using DS = DecodeSmem<FK, FV, D>;
+  // two decode tiles per CTA (one per half of its warps) where two rings of two
+  // stages fit, else one
+  static constexpr bool kTwoDecode = 2 * DS::total(2) <= 227 * 1024;
+  static constexpr int kDecodePerCta = kTwoDecode ? 2 : 1;
+  static constexpr int kDecNeed = kDecodePerCta * DS::total(2);
+  static constexpr int kNeed = ChunkSmem<FK, FV, D>::kTotal > kDecNeed ? ChunkSmem<FK, FV, D>::kTotal : kDecNeed;
+  static constexpr int kBytes = (kNeed + 255) / 256 * 256;
+  static constexpr int kHalfBytes = kBytes / kDecodePerCta;  // one decode tile's share (a multiple of 128)
+  static constexpr int kDecodeStages = DS::stages_for(kHalfBytes - 16);
+  static_assert(DS::total(kDecodeStages) <= kHalfBytes, "decode tile does not fit");
 };
 
 template <int FK, int FV, int D>
@@ -1007,9 +1019,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1) mixed_attention_kernel(AttnP
   if (tile < p.n_chunk_tiles) {
     chunk_tile<FK, FV, D>(p, p.tiles[tile], smem, err);
   } else {
-    if (threadIdx.x >= kThreads) return;  // a decode tile runs on 8 warps
-    decode_tile<FK, FV, D, FusedSmem<FK, FV, D>::kDecodeStages>(p, p.tiles[tile], tile - p.n_chunk_tiles, smem,
-                                                               err);
+    // two decode tiles per CTA where they fit, one on each half of its warps and
+    // shared memory; else one on the first half
+    using FS = FusedSmem<FK, FV, D>;
+    const int half = threadIdx.x >= kThreads ? 1 : 0;
+    if (half && !FS::kTwoDecode) return;
+    const int d = FS::kDecodePerCta * (tile - p.n_chunk_tiles) + half;
+    if (d >= p.n_decode_tiles) return;
+    decode_tile<FK, FV, D, FS::kDecodeStages>(p, p.tiles[p.n_chunk_tiles + d], d, smem + half * FS::kHalfBytes, err,
+                                              half);
   }
 }
 
@@ -1017,7 +1035,7 @@ template <int FK, int FV, int D, int MINB, int NS>
 __global__ void __launch_bounds__(kThreads, MINB) decode_attention_kernel(AttnParams p, unsigned int* err) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tile = blockIdx.x + p.n_chunk_tiles;
-  decode_tile<FK, FV, D, NS>(p, p.tiles[tile], blockIdx.x, smem, err);
+  decode_tile<FK, FV, D, NS>(p, p.tiles[tile], blockIdx.x, smem, err, 0);
 }
 
 template <int FK, int FV, int D>
@@ -1025,6 +1043,8 @@ cudaError_t launch_attention_t(const AttnParams& p, unsigned int* err, cudaStrea
   using DS = DecodeSmem<FK, FV, D>;
   const int n_tiles = p.n_chunk_tiles + p.n_decode_tiles;
   if (n_tiles == 0) return cudaSuccess;
+  constexpr int kPer = FusedSmem<FK, FV, D>::kDecodePerCta;  // decode tiles per fused CTA
+  const int n_fused_ctas = p.n_chunk_tiles + (p.n_decode_tiles + kPer - 1) / kPer;
   constexpr int kDec = DS::kTotal;
   constexpr int kFused = FusedSmem<FK, FV, D>::kBytes;
   auto* dec_kernel = decode_attention_kernel<FK, FV, D, DS::kSoloMinBlocks, DS::kSoloStages>;
@@ -1040,7 +1060,7 @@ cudaError_t launch_attention_t(const AttnParams& p, unsigned int* err, cudaStrea
   if (p.n_chunk_tiles == 0) {
     dec_kernel<<<p.n_decode_tiles, kThreads, kDec, s>>>(p, err);
   } else {
-    mixed_attention_kernel<FK, FV, D><<<n_tiles, kFusedThreads, kFused, s>>>(p, err);
+    mixed_attention_kernel<FK, FV, D><<<n_fused_ctas, kFusedThreads, kFused, s>>>(p, err);
   }
   return cudaGetLastError();
 }
