@@ -18,15 +18,15 @@
 // shared memory, split partials by the last CTA of the (row, kv head) to
 // finish (atomic ticket, no spin).
 //
-// Chunk tiles (tensor-bound): a CTA owns 128 rows = 128/G query tokens x G
-// heads of one kv head.  K/V pages arrive raw through 1-D bulk copies (TMA
-// engine) into two stages.  A dequant warp group turns them into
-// 128-byte-swizzled fp16 tiles -- an exact hi/lo pair for quantised formats,
-// since d*q needs up to 18 significant bits -- and issues S = Q K^T on
-// tcgen05.mma (Q and S in TMEM, one MMA per half); a softmax warp group, one
-// TMEM lane (query row) per thread, writes P as fp16 back into TMEM and issues
-// O += P V.  S is double-buffered so the next tile's QK and dequantisation
-// overlap this tile's softmax and PV.
+// Chunk tiles (tensor-bound): a CTA of 16 warps owns 128 rows = 128/G query
+// tokens x G heads of one kv head.  Two dequant warp groups load the raw K and V
+// bytes straight from the cache and write 128-byte-swizzled fp16 operand tiles
+// -- an exact hi/lo pair for quantised formats, since d*q needs up to 18
+// significant bits; one thread issues every tcgen05.mma (S = Q K^T and O += P V,
+// one MMA per half, Q, S, P and O in TMEM); a softmax warp group, one TMEM lane
+// (query row) per thread, turns S into P.  K and S are double-buffered and P has
+// its own columns, so QK of the next tile and the dequantisation overlap this
+// tile's softmax and PV.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -701,13 +701,14 @@ __device__ __noinline__ bool dequant_loop(const uint8_t* __restrict__ q_plane, c
 //   V group (warps 8-11): the same for V(j), into a single buffer, key half h
 //     once the PV MMAs of tile j-1 that read that half are done;
 //   softmax group (warps 0-3, thread i = TMEM lane i = query row i): reads
-//     S[j%2] twice (row max, then P = 2^(s - m) as fp16 written over the
-//     scores), waits for PV(j-1), rescales O when the row max moved;
+//     S[j%2] twice (row max, then P = 2^(s - m) as fp16 into the P columns,
+//     each key half once the PV(j-1) MMAs reading that half of P(j-1) are
+//     done), rescales O when the row max moved;
 //   MMA warp (warp 12, one thread): issues QK(j) into S[j%2] once K(j) is
-//     written and PV(j-2) has read the P that tile j-2 left there, then PV(j-1),
-//     each key half as soon as its V half is written.
+//     written (S[j%2] was read by the softmax of tile j-2 before PV(j-2) was
+//     issued), then PV(j-1), each key half as soon as its V half is written.
 // The MMA issue blocks its thread for about the MMA's duration, which is why
-// one warp does nothing else.  TMEM: Q (A operand, fp16) | S0 | S1 | O (fp32).
+// one warp does nothing else.  TMEM: Q | P (A operands, fp16) | S0 | S1 | O (fp32).
 // Every wait is bounded; a timeout in any role makes all of them leave their
 // loops.
 template <int FK, int FV, int D>
@@ -715,7 +716,7 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
                                            unsigned int* err) {
   using L = ChunkSmem<FK, FV, D>;
   constexpr uint32_t kTmemCols = 512;
-  constexpr uint32_t kQCol = 0, kSCol0 = 128, kSCol1 = 256, kOCol = 384;
+  constexpr uint32_t kQCol = 0, kPCol = 64, kSCol0 = 128, kSCol1 = 256, kOCol = 384;
   constexpr int kGroup = 128;          // threads per warp group
   constexpr int kBarSoftmax = 1, kBarK = 2, kBarV = 3;
 
@@ -818,7 +819,7 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
     const uint32_t ninf = __float_as_uint(-CUDART_INF_F);
     for (int j = 0; j < n_kv; ++j) {
       const int st = j & 1;
-      const uint32_t ph = (uint32_t)((j >> 1) & 1), ph_prev = (uint32_t)(((j - 1) >> 1) & 1);
+      const uint32_t ph = (uint32_t)((j >> 1) & 1);
       const uint32_t s_base = st ? kSCol1 : kSCol0;
       const uint32_t s_col = tmem + lane_base + s_base;
       ok = mbar_wait(&qk_done[st], ph, err) && ok;
@@ -848,9 +849,10 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
       const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * sl2);
       const float alpha = ex2(m_run - m_new);
       const float neg_m = -m_new;
-      // pass 2: P = 2^(s*scale - m) as fp16 over the consumed scores (chunk c of
-      // P lands on columns of chunks already read); row sums in fp32.  The
-      // scale-and-shift and the sums run on fp32 pairs.
+      // pass 2: P = 2^(s*scale - m) as fp16 into the P columns (keys 32c.. of
+      // chunk c), each key half once the PV(j-1) MMAs reading that half of
+      // P(j-1) are done; row sums in fp32.  The scale-and-shift and the sums run
+      // on fp32 pairs.
       const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(neg_m, neg_m);
       uint64_t sum_a = f2_pack(0.f, 0.f), sum_b = sum_a;
 #pragma unroll 1
@@ -874,7 +876,11 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
           pk[e >> 1] = pack_f16x2(p0, p1);
           pk[(e >> 1) + 1] = pack_f16x2(p2, p3);
         }
-        tmem_st16(s_col + 16 * c, pk);
+        if (j > 0 && (c & 1) == 0) {
+          ok = mbar_wait(&pvh_done[c >> 1], (uint32_t)((j - 1) & 1), err) && ok;
+          tc_fence_after();
+        }
+        tmem_st16(tmem + lane_base + kPCol + 16 * c, pk);
       }
       float sum0, sum1, sum2, sum3;
       f2_unpack(sum_a, sum0, sum1);
@@ -883,10 +889,8 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
       sum1 += sum3;
       l_run = l_run * alpha + (sum0 + sum1);
       m_run = m_new;
-      // the running O may be rescaled only once PV(j-1) has finished with it
+      // the running O: PV(j-1) has finished with it (its last half was waited above)
       if (j > 0) {
-        ok = mbar_wait(&pv_done[(j - 1) & 1], ph_prev, err) && ok;
-        tc_fence_after();
         if (__any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
 #pragma unroll 1
           for (int ch = 0; ch < D / 32; ++ch) {
@@ -943,8 +947,7 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
         const int st = j & 1;
         const uint32_t s_col = tmem + (st ? kSCol1 : kSCol0);
         ok = mbar_wait(&kdeq[st], (uint32_t)((j >> 1) & 1), err) && ok;  // K(j) written to buffer st
-        // S[st] holds P(j-2) until PV(j-2) has read it
-        if (j > 1) ok = mbar_wait(&pv_done[st], (uint32_t)(((j - 2) >> 1) & 1), err) && ok;
+        // S[st] is free: the softmax of tile j-2 finished reading it before PV(j-2) was issued
         if (!ok) break;
         tc_fence_after();
         const uint32_t kd = st ? dK1 : dK0;  // low descriptor word of K buffer st
@@ -961,7 +964,7 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
       if (j > 0) {
         const int jp = j - 1, sp = jp & 1;
         ok = mbar_wait(&sm_done[sp], (uint32_t)((jp >> 1) & 1), err) && ok;  // P(j-1) written, O rescaled
-        const uint32_t p_col = tmem + (sp ? kSCol1 : kSCol0);
+        const uint32_t p_col = tmem + kPCol;
 #pragma unroll
         for (int hv = 0; hv < 2; ++hv) {
           ok = mbar_wait(&vdeq[hv], (uint32_t)(jp & 1), err) && ok;  // V half hv of tile j-1 written
