@@ -10,7 +10,9 @@
 
 #include <algorithm>
 #include <cmath>
+#include <functional>
 #include <mutex>
+#include <queue>
 #include <vector>
 
 #include "internal.h"
@@ -80,8 +82,56 @@ struct Tiling {
   WorkspaceLayout L{};
 };
 
+// SMs of the current device (0 when it cannot be read: no chunk splitting).
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// Pieces per chunk tile of one chunk row: the key range of each of the row's
+// tiles is cut into s pieces (s = 1..4) when that shortens the row's share of
+// the launch, judged by placing the pieces heaviest first on the least-loaded
+// of n_sm SMs (one chunk CTA per SM).  A piece costs its KV tiles plus one for
+// its prologue and the merge; rows with a tile shorter than 8 KV tiles are
+// never cut.
+int chunk_split_factor(const std::vector<int64_t>& costs, int n_sm) {
+  if (n_sm <= 0 || costs.empty()) return 1;
+  int64_t min_cost = costs[0];
+  for (int64_t c : costs) min_cost = std::min(min_cost, c);
+  if (min_cost < 8) return 1;
+  auto makespan = [&](int s) {
+    std::vector<int64_t> pieces;
+    pieces.reserve(costs.size() * s);
+    for (int64_t c : costs)
+      for (int q = 0; q < s; ++q) pieces.push_back((c * (q + 1)) / s - (c * q) / s + (s > 1 ? 1 : 0));
+    std::sort(pieces.begin(), pieces.end(), std::greater<int64_t>());
+    std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>> load;
+    for (int i = 0; i < n_sm; ++i) load.push(0);
+    int64_t span = 0;
+    for (int64_t pc : pieces) {
+      const int64_t l = load.top() + pc;
+      load.pop();
+      load.push(l);
+      span = std::max(span, l);
+    }
+    return span;
+  };
+  int best = 1;
+  int64_t best_span = makespan(1);
+  for (int s = 2; s <= 4; ++s) {
+    const int64_t sp = makespan(s);
+    if (sp * 20 < best_span * 19) {  // at least 5% shorter
+      best = s;
+      best_span = sp;
+    }
+  }
+  return best;
+}
+
 int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* kinds, const int32_t* seq,
-                 const int32_t* off, int max_pages, Tiling* out) {
+                 const int32_t* off, int max_pages, int n_sm, Tiling* out) {
   if (n_rows <= 0 || !kinds || !seq || !off || max_pages <= 0) return MIXATTN_ERR_INVALID_ARG;
   if (hq <= 0 || hq % c.num_kv_heads != 0) return MIXATTN_ERR_INVALID_ARG;
   const int G = hq / c.num_kv_heads;
@@ -93,6 +143,7 @@ int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* k
   struct Chunk {
     TileDesc t;
     int64_t cost;
+    int split;
   };
   std::vector<Chunk> chunks;
   std::vector<TileDesc> decodes;
@@ -115,6 +166,7 @@ int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* k
     rows[r].n_splits = 0;
     const int64_t nq = s - o;
     if (kinds[r] == MIXATTN_ROW_CHUNK) {
+      const size_t first_chunk = chunks.size();
       for (int g = 0; g < hkv; ++g) {
         for (int64_t b = 0; b < nq; b += T) {
           Chunk ch;
@@ -122,11 +174,20 @@ int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* k
           ch.t.kvh = g;
           ch.t.begin = (int32_t)b;
           ch.t.count = (int32_t)std::min<int64_t>(T, nq - b);
+          ch.t.kv0 = ch.t.kv1 = ch.t.part = 0;
+          ch.t.nsplit = 1;
           const int64_t key_end = std::min<int64_t>(s, o + b + ch.t.count);
           ch.cost = (key_end + kChunkN - 1) / kChunkN;
+          ch.split = 1;
           chunks.push_back(ch);
         }
       }
+      // how far to cut this row's tiles depends on the row alone (and the GPU), so
+      // a row's result does not depend on the rest of the batch
+      std::vector<int64_t> costs;
+      for (size_t i = first_chunk; i < chunks.size(); ++i) costs.push_back(chunks[i].cost);
+      const int split = chunk_split_factor(costs, n_sm);
+      for (size_t i = first_chunk; i < chunks.size(); ++i) chunks[i].split = split;
     } else {
       const int pps = decode_pages_per_split((int)n_pages);
       const int ns = (int)((n_pages + pps - 1) / pps);
@@ -138,6 +199,8 @@ int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* k
           t.kvh = g;
           t.begin = sp * pps;
           t.count = (int32_t)std::min<int64_t>(pps, n_pages - (int64_t)sp * pps);
+          t.kv0 = t.kv1 = t.part = 0;
+          t.nsplit = 1;
           decodes.push_back(t);
         }
       }
@@ -145,21 +208,40 @@ int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* k
     total_q += nq;
     if (total_q > INT32_MAX / std::max(hq, 1)) return MIXATTN_ERR_INVALID_ARG;
   }
-  // heaviest chunk tiles first (they set the length of the launch)
+  // heaviest chunk tiles first (they set the length of the launch), each cut
+  // into `split` consecutive pieces of its key range
   std::stable_sort(chunks.begin(), chunks.end(), [](const Chunk& a, const Chunk& b) { return a.cost > b.cost; });
-  const int64_t n_tiles = (int64_t)chunks.size() + (int64_t)decodes.size();
+  int64_t n_pieces = 0;
+  bool any_split = false;
+  for (const Chunk& ch : chunks) {
+    n_pieces += ch.split;
+    any_split = any_split || ch.split > 1;
+  }
+  const int64_t n_tiles = n_pieces + (int64_t)decodes.size();
   if (n_tiles > INT32_MAX / 2) return MIXATTN_ERR_INVALID_ARG;
 
   Tiling& T2 = *out;
   T2.total_q = (int32_t)total_q;
-  T2.n_chunk = (int32_t)chunks.size();
+  T2.n_chunk = (int32_t)n_pieces;
   T2.n_decode = (int32_t)decodes.size();
-  T2.L = workspace_layout(n_rows, (int)n_tiles, T2.n_decode, hkv, G, c.head_dim);
+  T2.L = workspace_layout(n_rows, (int)n_tiles, T2.n_decode, hkv, G, c.head_dim, any_split);
   T2.image.assign(T2.L.upload_end - T2.L.rows, 0);
   memcpy(T2.image.data(), rows.data(), sizeof(RowInfo) * rows.size());
   TileDesc* td = reinterpret_cast<TileDesc*>(T2.image.data() + (T2.L.tiles - T2.L.rows));
-  for (size_t i = 0; i < chunks.size(); ++i) td[i] = chunks[i].t;
-  for (size_t i = 0; i < decodes.size(); ++i) td[chunks.size() + i] = decodes[i];
+  int64_t at = 0;
+  for (size_t i = 0; i < chunks.size(); ++i) {
+    const int64_t n_kv = chunks[i].cost;
+    const int split = chunks[i].split;
+    for (int q = 0; q < split; ++q) {
+      TileDesc t = chunks[i].t;
+      t.kv0 = (int32_t)((n_kv * q) / split);
+      t.kv1 = (int32_t)((n_kv * (q + 1)) / split);
+      t.part = q;
+      t.nsplit = split;
+      td[at++] = t;
+    }
+  }
+  for (size_t i = 0; i < decodes.size(); ++i) td[n_pieces + i] = decodes[i];
   // counters stay zero: every run starts its split tickets from 0
   return MIXATTN_OK;
 }
@@ -188,7 +270,7 @@ namespace {
 int plan_fill(mixattn_plan* p, int32_t n_rows, const int32_t* kinds, const int32_t* seq, const int32_t* off,
               int32_t max_pages, size_t* ws_bytes) {
   Tiling t;
-  int st = build_tiling(p->cache, p->hq, n_rows, kinds, seq, off, max_pages, &t);
+  int st = build_tiling(p->cache, p->hq, n_rows, kinds, seq, off, max_pages, device_sm_count(), &t);
   if (st != MIXATTN_OK) return st;
   // the previous run may still be copying from the pinned buffer
   if (p->copy_recorded) {
@@ -333,6 +415,8 @@ int mixattn_run(const mixattn_plan* plan_c, const void* q, const int32_t* page_t
   p.tiles = reinterpret_cast<const TileDesc*>(ws + L.tiles);
   p.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
   p.partials = reinterpret_cast<float*>(ws + L.partials);
+  p.chunk_partials = reinterpret_cast<float*>(ws + L.chunk_partials);
+  p.chunk_counters = p.counters + (size_t)plan->n_rows * c.num_kv_heads;
   p.max_pages = plan->max_pages;
   p.num_pages = c.num_pages;
   p.n_chunk_tiles = plan->tiling.n_chunk;
@@ -361,7 +445,7 @@ int mixattn_workspace_bytes(const mixattn_kv_cache* cache, int32_t num_q_heads, 
   if (st != MIXATTN_OK) return st;
   if (!workspace_bytes) return MIXATTN_ERR_INVALID_ARG;
   Tiling t;
-  st = build_tiling(*cache, num_q_heads, n_rows, row_kinds, seq_lens, q_offsets, max_pages, &t);
+  st = build_tiling(*cache, num_q_heads, n_rows, row_kinds, seq_lens, q_offsets, max_pages, device_sm_count(), &t);
   if (st != MIXATTN_OK) return st;
   *workspace_bytes = t.L.total;
   return MIXATTN_OK;

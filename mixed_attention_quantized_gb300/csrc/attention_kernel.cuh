@@ -712,7 +712,7 @@ __device__ __noinline__ bool dequant_loop(const uint8_t* __restrict__ q_plane, c
 // Every wait is bounded; a timeout in any role makes all of them leave their
 // loops.
 template <int FK, int FV, int D>
-__device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& t, uint8_t* smem_raw,
+__device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& t, int tile_idx, uint8_t* smem_raw,
                                            unsigned int* err) {
   using L = ChunkSmem<FK, FV, D>;
   constexpr uint32_t kTmemCols = 512;
@@ -741,7 +741,10 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
   const int n_pages_row = (ri.seq_len + kPage - 1) / kPage;
   // keys this tile can see: up to the position of its last query
   const int key_end = min(ri.seq_len, ri.q_offset + t.begin + t.count);
-  const int n_kv = (key_end + kChunkN - 1) / kChunkN;
+  // this piece walks KV tiles kv0 .. kv0 + n_kv - 1 (all of them unless the
+  // tile's key range is cut into pieces)
+  const int kv0 = t.kv0;
+  const int n_kv = t.kv1 - t.kv0;
   const int32_t* pt_row = p.page_table + (int64_t)t.row * p.max_pages;
 
   if (tid == 0) {
@@ -805,12 +808,16 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
     // =========== K group (warps 4-7) and V group (warps 8-11): dequantisation ===========
     const bool is_k = tid < 2 * kGroup;
     const bool done_ok =
-        is_k ? dequant_loop<FK, D, L::kKLo>(p.k_quant, p.k_scale, pt_row, n_pages_row, p.num_pages, p.hkv, g, key_end,
-                                            n_kv, tid - kGroup, true, smem + L::kK0, smem + L::kK0 + L::kTile,
+        is_k ? dequant_loop<FK, D, L::kKLo>(p.k_quant, p.k_scale, pt_row + kv0 * kPagesPerKvTile,
+                                            n_pages_row - kv0 * kPagesPerKvTile, p.num_pages, p.hkv, g,
+                                            key_end - kv0 * kChunkN, n_kv, tid - kGroup, true, smem + L::kK0,
+                                            smem + L::kK0 + L::kTile,
                                             smem + L::kK1, smem + L::kK1 + L::kTile, qk_done, kdeq, kBarK,
                                             abort_flag, err)
-             : dequant_loop<FV, D, L::kVLo>(p.v_quant, p.v_scale, pt_row, n_pages_row, p.num_pages, p.hkv, g, key_end,
-                                            n_kv, tid - 2 * kGroup, false, smem + L::kVh, smem + L::kVl, smem + L::kVh,
+             : dequant_loop<FV, D, L::kVLo>(p.v_quant, p.v_scale, pt_row + kv0 * kPagesPerKvTile,
+                                            n_pages_row - kv0 * kPagesPerKvTile, p.num_pages, p.hkv, g,
+                                            key_end - kv0 * kChunkN, n_kv, tid - 2 * kGroup, false, smem + L::kVh,
+                                            smem + L::kVl, smem + L::kVh,
                                             smem + L::kVl, pvh_done, vdeq, kBarV, abort_flag, err);
     if (!done_ok) *abort_flag = 1;
   } else if (tid < kGroup) {
@@ -824,7 +831,7 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
       const uint32_t s_col = tmem + lane_base + s_base;
       ok = mbar_wait(&qk_done[st], ph, err) && ok;
       tc_fence_after();
-      const int kbase = j * kChunkN;
+      const int kbase = (kv0 + j) * kChunkN;
       // causal mask: only a warp whose tile crosses the diagonal pays for it
       const bool diag = __any_sync(0xFFFFFFFFu, kbase + kChunkN - 1 > pos);
       uint32_t a[32];
@@ -847,8 +854,11 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
       }
       // running max in log2 units (the score scale is positive, so it commutes with max)
       const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * sl2);
-      const float alpha = ex2(m_run - m_new);
-      const float neg_m = -m_new;
+      // a row can see none of a piece's first keys (a later piece of a cut tile):
+      // everything stays zero until its first visible key
+      const bool none = m_new == -CUDART_INF_F;
+      const float alpha = none ? 1.f : ex2(m_run - m_new);
+      const float neg_m = none ? 0.f : -m_new;
       // pass 2: P = 2^(s*scale - m) as fp16 into the P columns (keys 32c.. of
       // chunk c), each key half once the PV(j-1) MMAs reading that half of
       // P(j-1) are done; row sums in fp32.  The scale-and-shift and the sums run
@@ -918,25 +928,82 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
     }
     // ---- epilogue: O / l -> fp16 ----
     const bool done = !*abort_flag;
-    if (done) ok = mbar_wait(&pv_done[(n_kv - 1) & 1], (uint32_t)(((n_kv - 1) >> 1) & 1), err) && ok;
+    if (done && n_kv > 0) ok = mbar_wait(&pv_done[(n_kv - 1) & 1], (uint32_t)(((n_kv - 1) >> 1) & 1), err) && ok;
     tc_fence_after();
-    const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
     uint16_t* dst = static_cast<uint16_t*>(p.o) +
                     ((int64_t)(ri.q_start + t.begin + tok) * p.hq + (int64_t)g * G + (row & (G - 1))) * D;
+    if (t.nsplit == 1) {
+      const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
 #pragma unroll 1
-    for (int ch = 0; ch < D / 32; ++ch) {
-      uint32_t v[32];
-      tmem_ld32(tmem + lane_base + kOCol + 32 * ch, v);
-      tmem_wait_ld();
-      uint32_t pk[16];
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + kOCol + 32 * ch, v);
+        tmem_wait_ld();
+        uint32_t pk[16];
 #pragma unroll
-      for (int e = 0; e < 32; e += 2)
-        pk[e >> 1] = pack_f16x2(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
-      if (row_valid && ok && done) {
+        for (int e = 0; e < 32; e += 2)
+          pk[e >> 1] = pack_f16x2(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
+        if (row_valid && ok && done) {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          *reinterpret_cast<uint4*>(dst + 32 * ch + 8 * q4) =
-              make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+          for (int q4 = 0; q4 < 4; ++q4)
+            *reinterpret_cast<uint4*>(dst + 32 * ch + 8 * q4) =
+                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+        }
+      }
+    } else {
+      // a piece of a cut tile: leave (m, l, unnormalised O) of its rows; the last
+      // piece to finish merges them (log-sum-exp) and writes O
+      const int64_t n_o = (int64_t)p.n_chunk_tiles * kChunkM * D;  // the O partials come first
+      float* o_part = p.chunk_partials + ((int64_t)tile_idx * kChunkM + row) * D;
+      float* ml_part = p.chunk_partials + n_o + ((int64_t)tile_idx * kChunkM + row) * 2;
+      ml_part[0] = m_run;
+      ml_part[1] = l_run;
+#pragma unroll 1
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + kOCol + 32 * ch, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          *reinterpret_cast<uint4*>(o_part + 32 * ch + 4 * q4) =
+              make_uint4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+      }
+      __threadfence();
+      __shared__ int s_last_piece;
+      bar_any(kBarSoftmax, kGroup, false);
+      const int first = tile_idx - t.part;  // the tile's pieces are consecutive
+      if (tid == 0) s_last_piece = atomicAdd(&p.chunk_counters[first], 1u) == (unsigned)(t.nsplit - 1);
+      bar_any(kBarSoftmax, kGroup, false);
+      if (s_last_piece) {
+        __threadfence();
+        float m_all = -CUDART_INF_F;
+        for (int q = 0; q < t.nsplit; ++q)
+          m_all = fmaxf(m_all, __ldcg(p.chunk_partials + n_o + ((int64_t)(first + q) * kChunkM + row) * 2));
+        float l_all = 0.f;
+        for (int q = 0; q < t.nsplit; ++q) {
+          const float* ml = p.chunk_partials + n_o + ((int64_t)(first + q) * kChunkM + row) * 2;
+          const float mq = __ldcg(ml);
+          l_all += mq == -CUDART_INF_F ? 0.f : __ldcg(ml + 1) * ex2(mq - m_all);
+        }
+        const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
+#pragma unroll 1
+        for (int d0 = 0; d0 < D; d0 += 8) {
+          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          for (int q = 0; q < t.nsplit; ++q) {
+            const float mq = __ldcg(p.chunk_partials + n_o + ((int64_t)(first + q) * kChunkM + row) * 2);
+            if (mq == -CUDART_INF_F) continue;
+            const float w = ex2(mq - m_all);
+            const float* op = p.chunk_partials + ((int64_t)(first + q) * kChunkM + row) * D + d0;
+            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(op));
+            const float4 x1 = __ldcg(reinterpret_cast<const float4*>(op + 4));
+            acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
+            acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
+          }
+          if (row_valid && ok && done)
+            *reinterpret_cast<uint4*>(dst + d0) =
+                make_uint4(pack_f16x2(acc[0] * inv_l, acc[1] * inv_l), pack_f16x2(acc[2] * inv_l, acc[3] * inv_l),
+                           pack_f16x2(acc[4] * inv_l, acc[5] * inv_l), pack_f16x2(acc[6] * inv_l, acc[7] * inv_l));
+        }
       }
     }
   } else if (tid == 3 * kGroup) {
@@ -1020,7 +1087,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) mixed_attention_kernel(AttnP
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tile = blockIdx.x;
   if (tile < p.n_chunk_tiles) {
-    chunk_tile<FK, FV, D>(p, p.tiles[tile], smem, err);
+    chunk_tile<FK, FV, D>(p, p.tiles[tile], tile, smem, err);
   } else {
     // two decode tiles per CTA where they fit, one on each half of its warps and
     // shared memory; else one on the first half

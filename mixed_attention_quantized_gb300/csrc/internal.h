@@ -27,6 +27,7 @@ constexpr int kFusedThreads = 512; // threads of a fused-launch CTA: three worki
                                    // the first kThreads
 constexpr int kChunkM = 128;       // rows (query tokens x group heads) of a chunk tile
 constexpr int kChunkN = 128;       // keys per KV tile of the chunk path (4 pages)
+constexpr int kPagesPerKvTile = kChunkN / kPage;
 constexpr int kMaxGroup = 8;       // q heads per kv head held in one mma N=8 tile
 
 // Per-row data the kernel needs (copied with the tile list).
@@ -38,13 +39,20 @@ struct RowInfo {
 };
 
 // One tile of work for one CTA.
-//   chunk:  queries begin .. begin+count-1 of `row` (count <= 128 / G), kv head kvh
-//   decode: pages begin .. begin+count-1 of `row`, kv head kvh
+//   chunk:  queries begin .. begin+count-1 of `row` (count <= 128 / G), kv head kvh,
+//           against 128-key KV tiles kv0 .. kv1-1; a tile whose key range is cut
+//           into nsplit pieces (part = 0 .. nsplit-1, consecutive in the tile
+//           list) leaves partial results that the last piece to finish merges
+//   decode: pages begin .. begin+count-1 of `row`, kv head kvh (kv0..nsplit unused)
 struct TileDesc {
   int32_t row;
   int32_t kvh;
   int32_t begin;
   int32_t count;
+  int32_t kv0;
+  int32_t kv1;
+  int32_t part;
+  int32_t nsplit;
 };
 
 // Pages each warp of a decode CTA walks, a function of the row's own length
@@ -66,25 +74,29 @@ MIXATTN_HD int scale_row_bytes(int fmt, int head_dim) {
 
 // Workspace layout of one plan (byte offsets from the workspace base).
 struct WorkspaceLayout {
-  size_t rows;       // RowInfo[n_rows]
-  size_t tiles;      // TileDesc[n_tiles]      (chunk tiles first)
-  size_t counters;   // uint32[n_rows * Hkv]  (zeroed by every run's copy)
-  size_t upload_end; // end of the block copied from the plan's host buffer
-  size_t partials;   // float[n_decode_tiles][G][head_dim + 2]
+  size_t rows;            // RowInfo[n_rows]
+  size_t tiles;           // TileDesc[n_tiles]      (chunk tiles first)
+  size_t counters;        // uint32[n_rows * Hkv + n_chunk_tiles]  (zeroed by every run's copy):
+                          // decode split tickets per (row, kv head), then chunk-piece tickets
+  size_t upload_end;      // end of the block copied from the plan's host buffer
+  size_t partials;        // float[n_decode_tiles][G][head_dim + 2]
+  size_t chunk_partials;  // float[n_chunk_tiles][128][head_dim + 2] when any chunk tile is split
   size_t total;
 };
 
 MIXATTN_HD size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 MIXATTN_HD WorkspaceLayout workspace_layout(int n_rows, int n_tiles, int n_decode_tiles, int hkv,
-                                            int group, int head_dim) {
+                                            int group, int head_dim, bool chunk_split) {
+  const size_t n_chunk = (size_t)(n_tiles - n_decode_tiles);
   WorkspaceLayout L;
   L.rows = 256;
   L.tiles = align_up(L.rows + sizeof(RowInfo) * (size_t)n_rows, 16);
   L.counters = align_up(L.tiles + sizeof(TileDesc) * (size_t)n_tiles, 16);
-  L.upload_end = align_up(L.counters + sizeof(uint32_t) * (size_t)n_rows * hkv, 16);
+  L.upload_end = align_up(L.counters + sizeof(uint32_t) * ((size_t)n_rows * hkv + n_chunk), 16);
   L.partials = align_up(L.upload_end, 256);
-  L.total = align_up(L.partials + sizeof(float) * (size_t)n_decode_tiles * group * (head_dim + 2), 256);
+  L.chunk_partials = align_up(L.partials + sizeof(float) * (size_t)n_decode_tiles * group * (head_dim + 2), 256);
+  L.total = align_up(L.chunk_partials + (chunk_split ? sizeof(float) * n_chunk * kChunkM * (head_dim + 2) : 0), 256);
   return L;
 }
 
@@ -99,8 +111,11 @@ struct AttnParams {
   const int32_t* page_table;  // [n_rows][max_pages]
   const RowInfo* rows;
   const TileDesc* tiles;
-  uint32_t* counters;         // [n_rows][hkv]
+  uint32_t* counters;         // [n_rows][hkv], then one per chunk tile (piece tickets)
   float* partials;            // [n_decode_tiles][group][D + 2]
+  float* chunk_partials;      // O [n_chunk_tiles][128][D], then (m, l) [n_chunk_tiles][128] of the
+                              // pieces of cut chunk tiles
+  uint32_t* chunk_counters;   // [n_chunk_tiles]: piece tickets, indexed by a tile's first piece
   int32_t max_pages;
   int32_t num_pages;
   int32_t n_chunk_tiles;

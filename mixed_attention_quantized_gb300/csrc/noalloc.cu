@@ -117,7 +117,8 @@ int tile_into_upload(const mixattn_kv_cache& c, int hq, int n_rows, const int32_
   }
   const int64_t n_tiles = n_chunk + n_decode;
   if (n_tiles > INT32_MAX / 2) return MIXATTN_ERR_INVALID_ARG;
-  const WorkspaceLayout L = workspace_layout(n_rows, (int)n_tiles, (int)n_decode, hkv, G, c.head_dim);
+  // this path never cuts chunk tiles (its scratch holds no chunk partials)
+  const WorkspaceLayout L = workspace_layout(n_rows, (int)n_tiles, (int)n_decode, hkv, G, c.head_dim, false);
   if (L.total > kStaticScratchBytes || L.upload_end - L.rows > kStaticUploadBytes) return MIXATTN_ERR_WORKSPACE;
 
   // second pass: write the image
@@ -134,15 +135,18 @@ int tile_into_upload(const mixattn_kv_cache& c, int hq, int n_rows, const int32_
     rows[r].n_splits = 0;
     if (kinds[r] == MIXATTN_ROW_CHUNK) {
       for (int g = 0; g < hkv; ++g)
-        for (int64_t b = 0; b < nq; b += T)
-          tiles[ic++] = TileDesc{r, g, (int32_t)b, (int32_t)std::min<int64_t>(T, nq - b)};
+        for (int64_t b = 0; b < nq; b += T) {
+          const int32_t cnt = (int32_t)std::min<int64_t>(T, nq - b);
+          const int64_t key_end = std::min<int64_t>(s, o + b + cnt);
+          tiles[ic++] = TileDesc{r, g, (int32_t)b, cnt, 0, (int32_t)((key_end + kChunkN - 1) / kChunkN), 0, 1};
+        }
     } else {
       const int pps = decode_pages_per_split((int)n_pages);
       const int ns = (int)((n_pages + pps - 1) / pps);
       rows[r].n_splits = ns;
       for (int g = 0; g < hkv; ++g)
         for (int sp = 0; sp < ns; ++sp)
-          tiles[id++] = TileDesc{r, g, sp * pps, (int32_t)std::min<int64_t>(pps, n_pages - (int64_t)sp * pps)};
+          tiles[id++] = TileDesc{r, g, sp * pps, (int32_t)std::min<int64_t>(pps, n_pages - (int64_t)sp * pps), 0, 0, 0, 1};
     }
     q0 += nq;
   }
@@ -208,6 +212,8 @@ extern "C" int mixattn_mixed_attention_noalloc(const mixattn_kv_cache* cache, in
   p.tiles = reinterpret_cast<const TileDesc*>(ws + L.tiles);
   p.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
   p.partials = reinterpret_cast<float*>(ws + L.partials);
+  p.chunk_partials = reinterpret_cast<float*>(ws + L.chunk_partials);
+  p.chunk_counters = p.counters + (size_t)n_rows * cache->num_kv_heads;
   p.max_pages = max_pages;
   p.num_pages = cache->num_pages;
   p.n_chunk_tiles = n_chunk;

@@ -156,3 +156,25 @@ def test_workspace_too_small_is_rejected():
     with pytest.raises(mq.MixattnError) as e:
         plan.run(q, torch.from_numpy(pt).cuda(), torch.empty_like(q), mq.alloc_workspace(plan.workspace_bytes - 256))
     assert e.value.status == mq.ERR_WORKSPACE
+
+
+def test_cut_chunk_tiles_match_oracle_and_stay_row_independent():
+    """A long chunk row with fewer tiles than SMs has the key range of each tile
+    cut into pieces whose partial results merge by log-sum-exp; the result still
+    matches the oracle, and the cut depends on the row alone, so the row's bits
+    are the same alone and in a batch."""
+    import torch
+    import mixed_attention_quantized_gb300 as mq
+    kf = vf = wl.FMT_Q8_0
+    rows = [(C, 8192 + 256, 8192), (D, 5000, 4999)]
+    w = wl.custom("cut", 32, 8, 128, kf, vf, 31, rows)
+    cache, pt = build_cache(w)
+    plan = mq.Plan(cache, 32, w.row_kinds, w.seq_lens, w.q_offsets, pt.shape[1])
+    assert plan.info()["chunk_tiles"] > 64  # 64 tiles (256 tokens x 8 kv heads / 32), cut
+    plan.close()
+    full = run_attention(w, cache, pt)
+    assert max_err(full, oracle_attention(w)) <= TOL
+    one = wl.custom("cut1", 32, 8, 128, kf, vf, 31, rows[:1])
+    q = torch.from_numpy(wl.queries(w)[:256].copy()).cuda()
+    alone = run_attention(one, cache, pt[:1], q=q)
+    assert np.array_equal(alone, full[:256])
