@@ -153,9 +153,13 @@ int mixattn_kv_export_blocks(const mixattn_kv_cache* cache, int32_t which, const
  * whose K/V must already be in the cache (append first, then attend).
  *
  * Tiles: chunk rows are cut into (kv head, 128/G query tokens x G heads)
- * tensor-core tiles, heaviest first; decode rows into (kv head, page range)
- * split-K tiles whose size depends only on the row's own length, so a row's
- * output bits do not depend on the rest of the batch.
+ * tensor-core tiles, heaviest first; when a chunk row has too few tiles to keep
+ * every SM of the current device busy to the end, the key range of each of its
+ * tiles is cut into 2-4 pieces whose partial results merge by log-sum-exp
+ * (a choice made from the row itself and the device's SM count).  Decode rows
+ * are cut into (kv head, page range) split-K tiles whose size depends only on
+ * the row's own length.  So a row's output bits do not depend on the rest of
+ * the batch.
  *
  *   num_q_heads      multiple of cache->num_kv_heads; G = num_q_heads /
  *                    num_kv_heads must be 1, 2, 4 or 8
@@ -176,7 +180,8 @@ int mixattn_plan_update(mixattn_plan* plan, int32_t n_rows, const int32_t* row_k
                         const int32_t* seq_lens, const int32_t* q_offsets, int32_t max_pages,
                         size_t* workspace_bytes);
 
-/* Total query tokens (rows of q and o) and tile counts of a plan. */
+/* Total query tokens (rows of q and o) and tile counts of a plan (every piece
+ * of a cut chunk tile counts as one chunk tile). */
 int mixattn_plan_info(const mixattn_plan* plan, int32_t* total_q, int32_t* n_chunk_tiles,
                       int32_t* n_decode_tiles);
 
@@ -233,9 +238,10 @@ int mixattn_workspace_bytes(const mixattn_kv_cache* cache, int32_t num_q_heads, 
  * every GPU that loads the library holds until the process exits, and the tile
  * list is staged in a library-owned host array.  No cudaMalloc, cudaFree,
  * cudaHostAlloc or other allocating routine is called.
- *   - A batch whose workspace (mixattn_workspace_bytes) exceeds 16 MiB -- at
- *     head_dim 128 and 4 q heads per kv head, about 8000 decode split tiles --
- *     returns MIXATTN_ERR_WORKSPACE and launches nothing.
+ *   - Chunk tiles are never cut into key-range pieces here (that would need
+ *     room for their partial results).  A batch whose remaining workspace
+ *     exceeds 16 MiB -- at head_dim 128 and 4 q heads per kv head, about 8000
+ *     decode split tiles -- returns MIXATTN_ERR_WORKSPACE and launches nothing.
  *   - The first call on a device looks up the array's device address (once per
  *     device, with that device current); make that first call before any stream
  *     capture.
