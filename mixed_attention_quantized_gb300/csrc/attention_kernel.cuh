@@ -718,7 +718,7 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kQCol = 0, kPCol = 64, kSCol0 = 128, kSCol1 = 256, kOCol = 384;
   constexpr int kGroup = 128;          // threads per warp group
-  constexpr int kBarSoftmax = 1, kBarK = 2, kBarV = 3;
+  constexpr int kBarSoftmax = 1, kBarK = 2, kBarV = 3, kBarQ = 4;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
@@ -788,9 +788,13 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
     }
     tmem_wait_st();
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+  // Q is in TMEM before the MMA warp issues QK(0); the dequant groups need
+  // neither, so their first loads overlap the Q load
+  if (tid < kGroup || warp == 12) {
+    tc_fence_before();
+    bar_any(kBarQ, kGroup + 32, false);
+    tc_fence_after();
+  }
 
   constexpr uint32_t kIdescQK = idesc_f16_f32(128, kChunkN, false, false);
   constexpr uint32_t kIdescPV = idesc_f16_f32(128, D, false, true);
