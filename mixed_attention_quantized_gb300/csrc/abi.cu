@@ -79,6 +79,7 @@ cudaError_t dispatch_attention(int k_fmt, int v_fmt, int head_dim, const AttnPar
 struct Tiling {
   std::vector<uint8_t> image;  // [rows | tiles | counters], from WorkspaceLayout::rows
   int32_t total_q = 0, n_chunk = 0, n_decode = 0;
+  int32_t chunk_kv_tiles = 0;  // KV tiles over all chunk tiles (their mean decides persistence)
   WorkspaceLayout L{};
 };
 
@@ -228,9 +229,10 @@ int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* k
   T2.image.assign(T2.L.upload_end - T2.L.rows, 0);
   memcpy(T2.image.data(), rows.data(), sizeof(RowInfo) * rows.size());
   TileDesc* td = reinterpret_cast<TileDesc*>(T2.image.data() + (T2.L.tiles - T2.L.rows));
-  int64_t at = 0;
+  int64_t at = 0, kv_tiles = 0;
   for (size_t i = 0; i < chunks.size(); ++i) {
     const int64_t n_kv = chunks[i].cost;
+    kv_tiles += n_kv;
     const int split = chunks[i].split;
     for (int q = 0; q < split; ++q) {
       TileDesc t = chunks[i].t;
@@ -242,6 +244,7 @@ int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* k
     }
   }
   for (size_t i = 0; i < decodes.size(); ++i) td[n_pieces + i] = decodes[i];
+  T2.chunk_kv_tiles = (int32_t)std::min<int64_t>(kv_tiles, INT32_MAX);
   // counters stay zero: every run starts its split tickets from 0
   return MIXATTN_OK;
 }
@@ -420,6 +423,7 @@ int mixattn_run(const mixattn_plan* plan_c, const void* q, const int32_t* page_t
   p.max_pages = plan->max_pages;
   p.num_pages = c.num_pages;
   p.n_chunk_tiles = plan->tiling.n_chunk;
+  p.chunk_kv_tiles = plan->tiling.chunk_kv_tiles;
   p.n_decode_tiles = plan->tiling.n_decode;
   p.hq = plan->hq;
   p.hkv = c.num_kv_heads;

@@ -29,6 +29,8 @@
 // tile's softmax and PV.
 #pragma once
 
+#include <algorithm>
+
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -631,20 +633,21 @@ __device__ __forceinline__ void convert_half(const HalfRaw<F, D>& r, uint8_t* __
   }
 }
 
-// The whole loop of one dequant group over the KV tiles of a chunk tile (one
+// The loop of one dequant group over the KV tiles of one chunk tile (one
 // out-of-line copy per format serves the K and the V group, which then share
-// instruction-cache lines).
-//   K group: K(j) goes to buffer j % 2 (hi at dst_hi[j%2], lo at dst_lo[j%2])
-//     once QK(j-2) has released it (qk_done[j%2]); after both halves it arrives
-//     on ready[j%2].
-//   V group: V(j) goes to the single buffer, half h once the PV MMAs of tile
-//     j-1 that read that half are done (pvh_done[h]); it arrives on ready[h]
+// instruction-cache lines).  Buffers and barrier phases follow the CTA's running
+// KV-tile count jg = jg0 + j, which continues across the CTA's chunk tiles.
+//   K group: K(jg) goes to buffer jg % 2 (hi at dst_hi[jg%2], lo at
+//     dst_lo[jg%2]) once QK(jg-2) has released it (qk_done[jg%2]); after both
+//     halves it arrives on ready[jg%2].
+//   V group: V(jg) goes to the single buffer, half h once the PV MMAs of tile
+//     jg-1 that read that half are done (pvh_done[h]); it arrives on ready[h]
 //     after each half.
 // Returns false when the group left early (a timeout here or elsewhere).
 template <int F, int D, bool LO>
 __device__ __noinline__ bool dequant_loop(const uint8_t* __restrict__ q_plane, const uint16_t* __restrict__ s_plane,
                                           const int32_t* __restrict__ pt_row, int n_pages_row, int num_pages,
-                                          int hkv, int g, int key_end, int n_kv, int t0, bool is_k,
+                                          int hkv, int g, int key_end, int n_kv, int jg0, int t0, bool is_k,
                                           uint8_t* dst_hi0, uint8_t* dst_lo0, uint8_t* dst_hi1, uint8_t* dst_lo1,
                                           uint64_t* free_bars, uint64_t* ready, int bar_id,
                                           volatile int* abort_flag, unsigned int* err) {
@@ -653,14 +656,16 @@ __device__ __noinline__ bool dequant_loop(const uint8_t* __restrict__ q_plane, c
   auto pid_of = [&](int pg) { return ldg_s32_or(pt_row + pg, pg < n_pages_row && pg * kPage < key_end, kNoPage); };
   auto valid_of = [&](int j, int h) { return key_end - j * kChunkN - h * (kChunkN / 2); };
   // one half: wait until its destination is free, convert, publish
+  // buffers and barrier phases follow the CTA's running KV-tile count jg0 + j
   auto process = [&](const HalfRaw<F, D>& r, int j, int h) -> bool {
+    const int jg = jg0 + j;
     if (is_k) {
-      if (h == 0 && j > 1) ok = mbar_wait(&free_bars[j & 1], (uint32_t)(((j - 2) >> 1) & 1), err) && ok;
+      if (h == 0 && jg > 1) ok = mbar_wait(&free_bars[jg & 1], (uint32_t)(((jg - 2) >> 1) & 1), err) && ok;
     } else {
-      if (j > 0) ok = mbar_wait(&free_bars[h], (uint32_t)((j - 1) & 1), err) && ok;
+      if (jg > 0) ok = mbar_wait(&free_bars[h], (uint32_t)((jg - 1) & 1), err) && ok;
     }
     tc_fence_after();
-    const bool b1 = is_k && (j & 1);
+    const bool b1 = is_k && (jg & 1);
     convert_half<F, D, LO>(r, b1 ? dst_hi1 : dst_hi0, b1 ? dst_lo1 : dst_lo0, h, t0);
     fence_proxy_async_smem();
     if (bar_any(bar_id, 128, !ok || *abort_flag)) {  // one decision for the group
@@ -669,7 +674,7 @@ __device__ __noinline__ bool dequant_loop(const uint8_t* __restrict__ q_plane, c
     }
     if (t0 == 0) {
       if (!is_k) mbar_arrive(&ready[h]);
-      else if (h == 1) mbar_arrive(&ready[j & 1]);
+      else if (h == 1) mbar_arrive(&ready[jg & 1]);
     }
     return true;
   };
@@ -693,59 +698,63 @@ __device__ __noinline__ bool dequant_loop(const uint8_t* __restrict__ q_plane, c
   return ok;
 }
 
-// Chunk tile: 128 rows (128/G query tokens x G heads of kv head `t.kvh`) against
-// the keys they can see, in 128-key KV tiles j.  Roles:
-//   K group (warps 4-7): loads the raw K bytes of tile j straight from the cache
-//     planes (one 64-key half ahead of their use) and dequantises K(j) into
-//     operand buffer j%2 once QK(j-2) has released it;
-//   V group (warps 8-11): the same for V(j), into a single buffer, key half h
-//     once the PV MMAs of tile j-1 that read that half are done;
+// Tile k of chunk CTA c among C chunk CTAs: a snake over the heaviest-first
+// tile list (c, 2C-1-c, 2C+c, ...), so every CTA gets a similar share of work;
+// -1 where the snake runs past the last tile.
+__device__ __forceinline__ int chunk_tile_of(int c, int k, int C, int n) {
+  const int idx = (k & 1) ? (k + 1) * C - 1 - c : k * C + c;
+  return idx < n ? idx : -1;
+}
+
+// Chunk CTA c of C: walks its chunk tiles (chunk_tile_of) one after the other.
+// A tile is 128 rows (128/G query tokens x G heads of kv head `t.kvh`) against
+// the keys they can see, in 128-key KV tiles.  Roles:
+//   K group (warps 4-7): loads the raw K bytes of each KV tile straight from the
+//     cache planes (one 64-key half ahead of their use) and dequantises them
+//     into operand buffer jg%2 once QK(jg-2) has released it;
+//   V group (warps 8-11): the same for V, into a single buffer, key half h once
+//     the PV MMAs of the previous KV tile that read that half are done;
 //   softmax group (warps 0-3, thread i = TMEM lane i = query row i): reads
-//     S[j%2] twice (row max, then P = 2^(s - m) as fp16 into the P columns,
-//     each key half once the PV(j-1) MMAs reading that half of P(j-1) are
-//     done), rescales O when the row max moved;
-//   MMA warp (warp 12, one thread): issues QK(j) into S[j%2] once K(j) is
-//     written (S[j%2] was read by the softmax of tile j-2 before PV(j-2) was
-//     issued), then PV(j-1), each key half as soon as its V half is written.
-// The MMA issue blocks its thread for about the MMA's duration, which is why
-// one warp does nothing else.  TMEM: Q | P (A operands, fp16) | S0 | S1 | O (fp32).
-// Every wait is bounded; a timeout in any role makes all of them leave their
-// loops.
+//     S[jg%2] twice (row max, then P = 2^(s - m) as fp16 into the P columns,
+//     each key half once the previous PV MMAs reading that half are done),
+//     rescales O when the row max moved; after a tile's last scores it writes
+//     the next tile's Q, then stores this tile's O;
+//   MMA warp (warp 12, one thread): issues QK(jg) into S[jg%2] once K(jg) is
+//     written (and, on a tile's first KV tile, its Q), then PV(jg-1), each key
+//     half as soon as its V half is written.
+// jg counts the KV tiles the CTA has walked, across its tiles: buffers and
+// barrier phases follow it, so the next tile's loads, dequantisation and first
+// QK overlap this tile's last softmax and its epilogue.  The MMA issue blocks
+// its thread for about the MMA's duration, which is why one warp does nothing
+// else.  TMEM: Q | P (A operands, fp16) | S0 | S1 | O (fp32).  Every wait is
+// bounded; a timeout in any role makes all of them leave their loops.
 template <int FK, int FV, int D>
-__device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& t, int tile_idx, uint8_t* smem_raw,
-                                           unsigned int* err) {
+__device__ __forceinline__ void chunk_cta(const AttnParams& p, int cta, int n_ctas, uint8_t* smem_raw,
+                                          unsigned int* err) {
   using L = ChunkSmem<FK, FV, D>;
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kQCol = 0, kPCol = 64, kSCol0 = 128, kSCol1 = 256, kOCol = 384;
   constexpr int kGroup = 128;          // threads per warp group
-  constexpr int kBarSoftmax = 1, kBarK = 2, kBarV = 3, kBarQ = 4;
+  constexpr int kBarSoftmax = 1, kBarK = 2, kBarV = 3;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint64_t* kdeq = bars;                   // [2] K(j) written to buffer j%2
-  uint64_t* vdeq = kdeq + 2;               // [2] V half h of the current tile written
+  uint64_t* kdeq = bars;                   // [2] K(jg) written to buffer jg%2
+  uint64_t* vdeq = kdeq + 2;               // [2] V half h of the current KV tile written
   uint64_t* pvh_done = vdeq + 2;           // [2] the PV MMAs reading V half h are done
-  uint64_t* qk_done = pvh_done + 2;        // [2] S[st] holds the scores of the tile; K buffer st free
-  uint64_t* pv_done = qk_done + 2;         // [2] PV of the tile done (P in S[st] read)
-  uint64_t* sm_done = pv_done + 2;         // [2] P of the tile written, O rescaled
-  uint64_t* mma_fin = sm_done + 2;         // [1] every MMA of the tile done
-  constexpr int kNumBars = 13;
+  uint64_t* qk_done = pvh_done + 2;        // [2] S[st] holds the scores of the KV tile
+  uint64_t* pv_done = qk_done + 2;         // [2] PV of the KV tile done
+  uint64_t* sm_done = pv_done + 2;         // [2] P of the KV tile written, O rescaled
+  uint64_t* q_ready = sm_done + 2;         // [1] Q of the CTA's next tile is in TMEM
+  uint64_t* mma_fin = q_ready + 1;         // [1] every MMA of the CTA done
+  constexpr int kNumBars = 14;
   static_assert(kNumBars * 8 + 8 <= L::kBarBytes, "barrier area too small");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kNumBars) + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int G = p.group, lg = p.log2_group;
-  const int g = t.kvh;
-  const RowInfo ri = p.rows[t.row];
-  const int n_pages_row = (ri.seq_len + kPage - 1) / kPage;
-  // keys this tile can see: up to the position of its last query
-  const int key_end = min(ri.seq_len, ri.q_offset + t.begin + t.count);
-  // this piece walks KV tiles kv0 .. kv0 + n_kv - 1 (all of them unless the
-  // tile's key range is cut into pieces)
-  const int kv0 = t.kv0;
-  const int n_kv = t.kv1 - t.kv0;
-  const int32_t* pt_row = p.page_table + (int64_t)t.row * p.max_pages;
+  const int n_rounds = (p.n_chunk_tiles + n_ctas - 1) / n_ctas;
 
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) mbar_init(bars + i, 1);
@@ -760,41 +769,8 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  // softmax state: thread i < 128 owns row i (TMEM lane i)
-  const int row = tid & 127;
-  const int tok = row >> lg;
-  const bool row_valid = tid < 128 && tok < t.count;
-  const int pos = ri.q_offset + t.begin + min(tok, t.count - 1);
+  const int row = tid & 127;  // softmax group: TMEM lane = query row
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-
-  // ---- Q row -> TMEM (the A operand of QK), two fp16 per column ----
-  if (tid < kGroup) {
-    const uint16_t* src = static_cast<const uint16_t*>(p.q) +
-                          ((int64_t)(ri.q_start + t.begin + min(tok, t.count - 1)) * p.hq + (int64_t)g * G +
-                           (row & (G - 1))) * D;
-#pragma unroll
-    for (int ch = 0; ch < D / 64; ++ch) {
-      uint32_t v[32];
-#pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) {
-        const uint4 w = tok < t.count ? ldg_u128(src + 64 * ch + 8 * q4) : make_uint4(0u, 0u, 0u, 0u);
-        v[4 * q4] = w.x;
-        v[4 * q4 + 1] = w.y;
-        v[4 * q4 + 2] = w.z;
-        v[4 * q4 + 3] = w.w;
-      }
-      tmem_st32(tmem + lane_base + kQCol + 32 * ch, v);
-    }
-    tmem_wait_st();
-  }
-  // Q is in TMEM before the MMA warp issues QK(0); the dequant groups need
-  // neither, so their first loads overlap the Q load
-  if (tid < kGroup || warp == 12) {
-    tc_fence_before();
-    bar_any(kBarQ, kGroup + 32, false);
-    tc_fence_after();
-  }
 
   constexpr uint32_t kIdescQK = idesc_f16_f32(128, kChunkN, false, false);
   constexpr uint32_t kIdescPV = idesc_f16_f32(128, D, false, true);
@@ -806,255 +782,331 @@ __device__ __forceinline__ void chunk_tile(const AttnParams& p, const TileDesc& 
   const uint32_t dV = (uint32_t)sw128_desc(smem_u32(smem + L::kVh), kChunkN * 128, 1024);
   const uint32_t dHiV = (uint32_t)(sw128_desc(0, kChunkN * 128, 1024) >> 32);
   bool ok = true;
-  float m_run = -CUDART_INF_F, l_run = 0.f;
 
   if (tid >= kGroup && tid < 3 * kGroup) {
     // =========== K group (warps 4-7) and V group (warps 8-11): dequantisation ===========
     const bool is_k = tid < 2 * kGroup;
-    const bool done_ok =
-        is_k ? dequant_loop<FK, D, L::kKLo>(p.k_quant, p.k_scale, pt_row + kv0 * kPagesPerKvTile,
-                                            n_pages_row - kv0 * kPagesPerKvTile, p.num_pages, p.hkv, g,
-                                            key_end - kv0 * kChunkN, n_kv, tid - kGroup, true, smem + L::kK0,
-                                            smem + L::kK0 + L::kTile,
-                                            smem + L::kK1, smem + L::kK1 + L::kTile, qk_done, kdeq, kBarK,
-                                            abort_flag, err)
-             : dequant_loop<FV, D, L::kVLo>(p.v_quant, p.v_scale, pt_row + kv0 * kPagesPerKvTile,
-                                            n_pages_row - kv0 * kPagesPerKvTile, p.num_pages, p.hkv, g,
-                                            key_end - kv0 * kChunkN, n_kv, tid - 2 * kGroup, false, smem + L::kVh,
-                                            smem + L::kVl, smem + L::kVh,
-                                            smem + L::kVl, pvh_done, vdeq, kBarV, abort_flag, err);
-    if (!done_ok) *abort_flag = 1;
+    int jg0 = 0;
+    bool alive = true;
+    for (int k = 0; alive && k < n_rounds; ++k) {
+      const int idx = chunk_tile_of(cta, k, n_ctas, p.n_chunk_tiles);
+      if (idx < 0) continue;
+      const TileDesc t = p.tiles[idx];
+      const RowInfo ri = p.rows[t.row];
+      const int n_pages_row = (ri.seq_len + kPage - 1) / kPage;
+      const int key_end = min(ri.seq_len, ri.q_offset + t.begin + t.count);
+      const int kv0 = t.kv0, n_kv = t.kv1 - t.kv0;
+      const int32_t* pt_row = p.page_table + (int64_t)t.row * p.max_pages + kv0 * kPagesPerKvTile;
+      alive = is_k ? dequant_loop<FK, D, L::kKLo>(p.k_quant, p.k_scale, pt_row, n_pages_row - kv0 * kPagesPerKvTile,
+                                                  p.num_pages, p.hkv, t.kvh, key_end - kv0 * kChunkN, n_kv, jg0,
+                                                  tid - kGroup, true, smem + L::kK0, smem + L::kK0 + L::kTile,
+                                                  smem + L::kK1, smem + L::kK1 + L::kTile, qk_done, kdeq, kBarK,
+                                                  abort_flag, err)
+                   : dequant_loop<FV, D, L::kVLo>(p.v_quant, p.v_scale, pt_row, n_pages_row - kv0 * kPagesPerKvTile,
+                                                  p.num_pages, p.hkv, t.kvh, key_end - kv0 * kChunkN, n_kv, jg0,
+                                                  tid - 2 * kGroup, false, smem + L::kVh, smem + L::kVl,
+                                                  smem + L::kVh, smem + L::kVl, pvh_done, vdeq, kBarV, abort_flag,
+                                                  err);
+      jg0 += n_kv;
+    }
+    if (!alive) *abort_flag = 1;
   } else if (tid < kGroup) {
     // ======================= softmax group =======================
     const float sl2 = p.scale_log2;
     const uint32_t ninf = __float_as_uint(-CUDART_INF_F);
-    for (int j = 0; j < n_kv; ++j) {
-      const int st = j & 1;
-      const uint32_t ph = (uint32_t)((j >> 1) & 1);
-      const uint32_t s_base = st ? kSCol1 : kSCol0;
-      const uint32_t s_col = tmem + lane_base + s_base;
-      ok = mbar_wait(&qk_done[st], ph, err) && ok;
-      tc_fence_after();
-      const int kbase = (kv0 + j) * kChunkN;
-      // causal mask: only a warp whose tile crosses the diagonal pays for it
-      const bool diag = __any_sync(0xFFFFFFFFu, kbase + kChunkN - 1 > pos);
-      uint32_t a[32];
-      // pass 1: the row max of the tile's 128 scores, 32 at a time
-      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(s_col + 32 * c, a);
-        tmem_wait_ld();
-        if (diag) {
+    const int tok = row >> lg;
+    // Q rows of chunk tile idx -> TMEM (the A operand of QK), two fp16 per
+    // column; then the MMA warp may issue the tile's QK
+    auto write_q = [&](int idx) {
+      const TileDesc t = p.tiles[idx];
+      const RowInfo ri = p.rows[t.row];
+      const uint16_t* src = static_cast<const uint16_t*>(p.q) +
+                            ((int64_t)(ri.q_start + t.begin + min(tok, t.count - 1)) * p.hq + (int64_t)t.kvh * G +
+                             (row & (G - 1))) * D;
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (kbase + 32 * c + e > pos) a[e] = ninf;
-        }
+      for (int ch = 0; ch < D / 64; ++ch) {
+        uint32_t v[32];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          mx0 = fmax3(mx0, __uint_as_float(a[e]), __uint_as_float(a[e + 1]));
-          mx1 = fmax3(mx1, __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const uint4 w = tok < t.count ? ldg_u128(src + 64 * ch + 8 * q4) : make_uint4(0u, 0u, 0u, 0u);
+          v[4 * q4] = w.x;
+          v[4 * q4 + 1] = w.y;
+          v[4 * q4 + 2] = w.z;
+          v[4 * q4 + 3] = w.w;
         }
-      }
-      // running max in log2 units (the score scale is positive, so it commutes with max)
-      const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * sl2);
-      // a row can see none of a piece's first keys (a later piece of a cut tile):
-      // everything stays zero until its first visible key
-      const bool none = m_new == -CUDART_INF_F;
-      const float alpha = none ? 1.f : ex2(m_run - m_new);
-      const float neg_m = none ? 0.f : -m_new;
-      // pass 2: P = 2^(s*scale - m) as fp16 into the P columns (keys 32c.. of
-      // chunk c), each key half once the PV(j-1) MMAs reading that half of
-      // P(j-1) are done; row sums in fp32.  The scale-and-shift and the sums run
-      // on fp32 pairs.
-      const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(neg_m, neg_m);
-      uint64_t sum_a = f2_pack(0.f, 0.f), sum_b = sum_a;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(s_col + 32 * c, a);
-        tmem_wait_ld();
-        if (diag) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (kbase + 32 * c + e > pos) a[e] = ninf;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          float x0, x1, x2, x3;
-          f2_unpack(ffma2(f2_pack(__uint_as_float(a[e]), __uint_as_float(a[e + 1])), sl2x2, negm2), x0, x1);
-          f2_unpack(ffma2(f2_pack(__uint_as_float(a[e + 2]), __uint_as_float(a[e + 3])), sl2x2, negm2), x2, x3);
-          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-          sum_a = fadd2(sum_a, f2_pack(p0, p1));
-          sum_b = fadd2(sum_b, f2_pack(p2, p3));
-          pk[e >> 1] = pack_f16x2(p0, p1);
-          pk[(e >> 1) + 1] = pack_f16x2(p2, p3);
-        }
-        if (j > 0 && (c & 1) == 0) {
-          ok = mbar_wait(&pvh_done[c >> 1], (uint32_t)((j - 1) & 1), err) && ok;
-          tc_fence_after();
-        }
-        tmem_st16(tmem + lane_base + kPCol + 16 * c, pk);
-      }
-      float sum0, sum1, sum2, sum3;
-      f2_unpack(sum_a, sum0, sum1);
-      f2_unpack(sum_b, sum2, sum3);
-      sum0 += sum2;
-      sum1 += sum3;
-      l_run = l_run * alpha + (sum0 + sum1);
-      m_run = m_new;
-      // the running O: PV(j-1) has finished with it (its last half was waited above)
-      if (j > 0) {
-        if (__any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
-#pragma unroll 1
-          for (int ch = 0; ch < D / 32; ++ch) {
-            tmem_ld32(tmem + lane_base + kOCol + 32 * ch, a);
-            tmem_wait_ld();
-            const uint64_t al2 = f2_pack(alpha, alpha);
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float y0, y1;
-              f2_unpack(fmul2(f2_pack(__uint_as_float(a[e]), __uint_as_float(a[e + 1])), al2), y0, y1);
-              a[e] = __float_as_uint(y0);
-              a[e + 1] = __float_as_uint(y1);
-            }
-            tmem_st32(tmem + lane_base + kOCol + 32 * ch, a);
-          }
-        }
+        tmem_st32(tmem + lane_base + kQCol + 32 * ch, v);
       }
       tmem_wait_st();
       tc_fence_before();
-      if (bar_any(kBarSoftmax, kGroup, !ok || *abort_flag)) {  // one decision for the group
-        *abort_flag = 1;
-        break;
-      }
-      if (tid == 0) mbar_arrive(&sm_done[st]);  // P(j) written, O rescaled
-    }
-    // ---- epilogue: O / l -> fp16 ----
-    const bool done = !*abort_flag;
-    if (done && n_kv > 0) ok = mbar_wait(&pv_done[(n_kv - 1) & 1], (uint32_t)(((n_kv - 1) >> 1) & 1), err) && ok;
-    tc_fence_after();
-    uint16_t* dst = static_cast<uint16_t*>(p.o) +
-                    ((int64_t)(ri.q_start + t.begin + tok) * p.hq + (int64_t)g * G + (row & (G - 1))) * D;
-    if (t.nsplit == 1) {
-      const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kOCol + 32 * ch, v);
-        tmem_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2)
-          pk[e >> 1] = pack_f16x2(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
-        if (row_valid && ok && done) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            *reinterpret_cast<uint4*>(dst + 32 * ch + 8 * q4) =
-                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-        }
-      }
-    } else {
-      // a piece of a cut tile: leave (m, l, unnormalised O) of its rows; the last
-      // piece to finish merges them (log-sum-exp) and writes O
-      const int64_t n_o = (int64_t)p.n_chunk_tiles * kChunkM * D;  // the O partials come first
-      float* o_part = p.chunk_partials + ((int64_t)tile_idx * kChunkM + row) * D;
-      float* ml_part = p.chunk_partials + n_o + ((int64_t)tile_idx * kChunkM + row) * 2;
-      ml_part[0] = m_run;
-      ml_part[1] = l_run;
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kOCol + 32 * ch, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-          *reinterpret_cast<uint4*>(o_part + 32 * ch + 4 * q4) =
-              make_uint4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
-      }
-      __threadfence();
-      __shared__ int s_last_piece;
       bar_any(kBarSoftmax, kGroup, false);
-      const int first = tile_idx - t.part;  // the tile's pieces are consecutive
-      if (tid == 0) s_last_piece = atomicAdd(&p.chunk_counters[first], 1u) == (unsigned)(t.nsplit - 1);
-      bar_any(kBarSoftmax, kGroup, false);
-      if (s_last_piece) {
-        __threadfence();
-        float m_all = -CUDART_INF_F;
-        for (int q = 0; q < t.nsplit; ++q)
-          m_all = fmaxf(m_all, __ldcg(p.chunk_partials + n_o + ((int64_t)(first + q) * kChunkM + row) * 2));
-        float l_all = 0.f;
-        for (int q = 0; q < t.nsplit; ++q) {
-          const float* ml = p.chunk_partials + n_o + ((int64_t)(first + q) * kChunkM + row) * 2;
-          const float mq = __ldcg(ml);
-          l_all += mq == -CUDART_INF_F ? 0.f : __ldcg(ml + 1) * ex2(mq - m_all);
-        }
-        const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
+      if (tid == 0) mbar_arrive(q_ready);
+    };
+    auto next_round = [&](int k) {  // the first round >= k that holds a tile of this CTA
+      while (k < n_rounds && chunk_tile_of(cta, k, n_ctas, p.n_chunk_tiles) < 0) ++k;
+      return k;
+    };
+    int k = next_round(0);
+    if (k < n_rounds) write_q(chunk_tile_of(cta, k, n_ctas, p.n_chunk_tiles));
+    int jg0 = 0;
+    for (; k < n_rounds && !*abort_flag; k = next_round(k + 1)) {
+      const int idx = chunk_tile_of(cta, k, n_ctas, p.n_chunk_tiles);
+      const TileDesc t = p.tiles[idx];
+      const RowInfo ri = p.rows[t.row];
+      const int g = t.kvh;
+      const bool row_valid = tok < t.count;
+      const int pos = ri.q_offset + t.begin + min(tok, t.count - 1);
+      const int kv0 = t.kv0, n_kv = t.kv1 - t.kv0;
+      float m_run = -CUDART_INF_F, l_run = 0.f;
+      for (int j = 0; j < n_kv; ++j) {
+        const int jg = jg0 + j;
+        const int st = jg & 1;
+        const uint32_t ph = (uint32_t)((jg >> 1) & 1);
+        const uint32_t s_base = st ? kSCol1 : kSCol0;
+        const uint32_t s_col = tmem + lane_base + s_base;
+        ok = mbar_wait(&qk_done[st], ph, err) && ok;
+        tc_fence_after();
+        const int kbase = (kv0 + j) * kChunkN;
+        // causal mask: only a warp whose tile crosses the diagonal pays for it
+        const bool diag = __any_sync(0xFFFFFFFFu, kbase + kChunkN - 1 > pos);
+        uint32_t a[32];
+        // pass 1: the row max of the tile's 128 scores, 32 at a time
+        float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
 #pragma unroll 1
-        for (int d0 = 0; d0 < D; d0 += 8) {
-          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          for (int q = 0; q < t.nsplit; ++q) {
-            const float mq = __ldcg(p.chunk_partials + n_o + ((int64_t)(first + q) * kChunkM + row) * 2);
-            if (mq == -CUDART_INF_F) continue;
-            const float w = ex2(mq - m_all);
-            const float* op = p.chunk_partials + ((int64_t)(first + q) * kChunkM + row) * D + d0;
-            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(op));
-            const float4 x1 = __ldcg(reinterpret_cast<const float4*>(op + 4));
-            acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
-            acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(s_col + 32 * c, a);
+          tmem_wait_ld();
+          if (diag) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (kbase + 32 * c + e > pos) a[e] = ninf;
           }
-          if (row_valid && ok && done)
-            *reinterpret_cast<uint4*>(dst + d0) =
-                make_uint4(pack_f16x2(acc[0] * inv_l, acc[1] * inv_l), pack_f16x2(acc[2] * inv_l, acc[3] * inv_l),
-                           pack_f16x2(acc[4] * inv_l, acc[5] * inv_l), pack_f16x2(acc[6] * inv_l, acc[7] * inv_l));
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            mx0 = fmax3(mx0, __uint_as_float(a[e]), __uint_as_float(a[e + 1]));
+            mx1 = fmax3(mx1, __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
+          }
+        }
+        // running max in log2 units (the score scale is positive, so it commutes with max)
+        const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * sl2);
+        // a row can see none of a piece's first keys (a later piece of a cut tile):
+        // everything stays zero until its first visible key
+        const bool none = m_new == -CUDART_INF_F;
+        const float alpha = none ? 1.f : ex2(m_run - m_new);
+        const float neg_m = none ? 0.f : -m_new;
+        // pass 2: P = 2^(s*scale - m) as fp16 into the P columns (keys 32c.. of
+        // chunk c), each key half once the PV(j-1) MMAs reading that half of
+        // P(j-1) are done; row sums in fp32.  The scale-and-shift and the sums run
+        // on fp32 pairs.
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(neg_m, neg_m);
+        uint64_t sum_a = f2_pack(0.f, 0.f), sum_b = sum_a;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(s_col + 32 * c, a);
+          tmem_wait_ld();
+          if (diag) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (kbase + 32 * c + e > pos) a[e] = ninf;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            float x0, x1, x2, x3;
+            f2_unpack(ffma2(f2_pack(__uint_as_float(a[e]), __uint_as_float(a[e + 1])), sl2x2, negm2), x0, x1);
+            f2_unpack(ffma2(f2_pack(__uint_as_float(a[e + 2]), __uint_as_float(a[e + 3])), sl2x2, negm2), x2, x3);
+            const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+            sum_a = fadd2(sum_a, f2_pack(p0, p1));
+            sum_b = fadd2(sum_b, f2_pack(p2, p3));
+            pk[e >> 1] = pack_f16x2(p0, p1);
+            pk[(e >> 1) + 1] = pack_f16x2(p2, p3);
+          }
+          if (jg > 0 && (c & 1) == 0) {
+            ok = mbar_wait(&pvh_done[c >> 1], (uint32_t)((jg - 1) & 1), err) && ok;
+            tc_fence_after();
+          }
+          tmem_st16(tmem + lane_base + kPCol + 16 * c, pk);
+        }
+        float sum0, sum1, sum2, sum3;
+        f2_unpack(sum_a, sum0, sum1);
+        f2_unpack(sum_b, sum2, sum3);
+        sum0 += sum2;
+        sum1 += sum3;
+        l_run = l_run * alpha + (sum0 + sum1);
+        m_run = m_new;
+        // the running O: PV(j-1) has finished with it (its last half was waited above)
+        if (j > 0) {
+          if (__any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+#pragma unroll 1
+            for (int ch = 0; ch < D / 32; ++ch) {
+              tmem_ld32(tmem + lane_base + kOCol + 32 * ch, a);
+              tmem_wait_ld();
+              const uint64_t al2 = f2_pack(alpha, alpha);
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                float y0, y1;
+                f2_unpack(fmul2(f2_pack(__uint_as_float(a[e]), __uint_as_float(a[e + 1])), al2), y0, y1);
+                a[e] = __float_as_uint(y0);
+                a[e + 1] = __float_as_uint(y1);
+              }
+              tmem_st32(tmem + lane_base + kOCol + 32 * ch, a);
+            }
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        if (bar_any(kBarSoftmax, kGroup, !ok || *abort_flag)) {  // one decision for the group
+          *abort_flag = 1;
+          break;
+        }
+        if (tid == 0) mbar_arrive(&sm_done[st]);  // P(jg) written, O rescaled
+      }
+      // the next tile's Q: this tile's last QK is done (its scores were read above)
+      const int kn = next_round(k + 1);
+      if (kn < n_rounds && !*abort_flag) write_q(chunk_tile_of(cta, kn, n_ctas, p.n_chunk_tiles));
+      // ---- epilogue of this tile, while the MMA warp starts the next ----
+      const bool done = !*abort_flag;
+      const int jl = jg0 + n_kv - 1;  // the tile's last KV tile
+      if (done && n_kv > 0) ok = mbar_wait(&pv_done[jl & 1], (uint32_t)((jl >> 1) & 1), err) && ok;
+      tc_fence_after();
+      uint16_t* dst = static_cast<uint16_t*>(p.o) +
+                      ((int64_t)(ri.q_start + t.begin + tok) * p.hq + (int64_t)g * G + (row & (G - 1))) * D;
+      if (t.nsplit == 1) {
+        const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + kOCol + 32 * ch, v);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            pk[e >> 1] = pack_f16x2(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
+          if (row_valid && ok && done) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              *reinterpret_cast<uint4*>(dst + 32 * ch + 8 * q4) =
+                  make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+          }
+        }
+      } else {
+        // a piece of a cut tile: leave (m, l, unnormalised O) of its rows; the last
+        // piece to finish merges them (log-sum-exp) and writes O
+        const int64_t n_o = (int64_t)p.n_chunk_tiles * kChunkM * D;  // the O partials come first
+        float* o_part = p.chunk_partials + ((int64_t)idx * kChunkM + row) * D;
+        float* ml_part = p.chunk_partials + n_o + ((int64_t)idx * kChunkM + row) * 2;
+        ml_part[0] = m_run;
+        ml_part[1] = l_run;
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + kOCol + 32 * ch, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4)
+            *reinterpret_cast<uint4*>(o_part + 32 * ch + 4 * q4) =
+                make_uint4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+        }
+        __threadfence();
+        __shared__ int s_last_piece;
+        bar_any(kBarSoftmax, kGroup, false);
+        const int first = idx - t.part;  // the tile's pieces are consecutive
+        if (tid == 0) s_last_piece = atomicAdd(&p.chunk_counters[first], 1u) == (unsigned)(t.nsplit - 1);
+        bar_any(kBarSoftmax, kGroup, false);
+        if (s_last_piece) {
+          __threadfence();
+          float m_all = -CUDART_INF_F;
+          for (int q = 0; q < t.nsplit; ++q)
+            m_all = fmaxf(m_all, __ldcg(p.chunk_partials + n_o + ((int64_t)(first + q) * kChunkM + row) * 2));
+          float l_all = 0.f;
+          for (int q = 0; q < t.nsplit; ++q) {
+            const float* ml = p.chunk_partials + n_o + ((int64_t)(first + q) * kChunkM + row) * 2;
+            const float mq = __ldcg(ml);
+            l_all += mq == -CUDART_INF_F ? 0.f : __ldcg(ml + 1) * ex2(mq - m_all);
+          }
+          const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
+#pragma unroll 1
+          for (int d0 = 0; d0 < D; d0 += 8) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int q = 0; q < t.nsplit; ++q) {
+              const float mq = __ldcg(p.chunk_partials + n_o + ((int64_t)(first + q) * kChunkM + row) * 2);
+              if (mq == -CUDART_INF_F) continue;
+              const float w = ex2(mq - m_all);
+              const float* op = p.chunk_partials + ((int64_t)(first + q) * kChunkM + row) * D + d0;
+              const float4 x0 = __ldcg(reinterpret_cast<const float4*>(op));
+              const float4 x1 = __ldcg(reinterpret_cast<const float4*>(op + 4));
+              acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
+              acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
+            }
+            if (row_valid && ok && done)
+              *reinterpret_cast<uint4*>(dst + d0) =
+                  make_uint4(pack_f16x2(acc[0] * inv_l, acc[1] * inv_l), pack_f16x2(acc[2] * inv_l, acc[3] * inv_l),
+                             pack_f16x2(acc[4] * inv_l, acc[5] * inv_l), pack_f16x2(acc[6] * inv_l, acc[7] * inv_l));
+          }
         }
       }
+      jg0 += n_kv;
     }
   } else if (tid == 3 * kGroup) {
     // ============ MMA warp (warp 12, one thread): issues every tcgen05.mma ============
-    // Order on the tensor pipe: QK(0), QK(1), PV(0), QK(2), PV(1), ...
-    for (int j = 0; j <= n_kv; ++j) {
-      if (j < n_kv) {
-        const int st = j & 1;
-        const uint32_t s_col = tmem + (st ? kSCol1 : kSCol0);
-        ok = mbar_wait(&kdeq[st], (uint32_t)((j >> 1) & 1), err) && ok;  // K(j) written to buffer st
-        // S[st] is free: the softmax of tile j-2 finished reading it before PV(j-2) was issued
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kd = st ? dK1 : dK0;  // low descriptor word of K buffer st
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (uint32_t)((ks >> 2) * (kChunkN * 128) + (ks & 3) * 32) >> 4;
-          if (ks == 0) tc_mma_ts_w<0>(s_col, tmem + kQCol, kd + off, dHiK, kIdescQK);
-          else tc_mma_ts_w<1>(s_col, tmem + kQCol + 8 * ks, kd + off, dHiK, kIdescQK);
-          if (L::kKLo) tc_mma_ts_w<1>(s_col, tmem + kQCol + 8 * ks, kd + (L::kTile >> 4) + off, dHiK, kIdescQK);
-        }
-        if (!ok) break;
-        tc_commit(&qk_done[st]);
-      }
-      if (j > 0) {
-        const int jp = j - 1, sp = jp & 1;
-        ok = mbar_wait(&sm_done[sp], (uint32_t)((jp >> 1) & 1), err) && ok;  // P(j-1) written, O rescaled
-        const uint32_t p_col = tmem + kPCol;
-#pragma unroll
-        for (int hv = 0; hv < 2; ++hv) {
-          ok = mbar_wait(&vdeq[hv], (uint32_t)(jp & 1), err) && ok;  // V half hv of tile j-1 written
+    // Order on the tensor pipe: QK(0), QK(1), PV(0), QK(2), PV(1), ... over the
+    // CTA's KV tiles, the first QK of a tile once its Q is in TMEM.
+    int jg0 = 0, nt = 0;
+    for (int k = 0; k < n_rounds && ok; ++k) {
+      const int idx = chunk_tile_of(cta, k, n_ctas, p.n_chunk_tiles);
+      if (idx < 0) continue;
+      const TileDesc t = p.tiles[idx];
+      const int n_kv = t.kv1 - t.kv0;
+      ok = mbar_wait(q_ready, (uint32_t)(nt & 1), err) && ok;  // this tile's Q written
+      ++nt;
+      if (!ok) break;
+      tc_fence_after();
+      for (int j = 0; j <= n_kv; ++j) {
+        if (j < n_kv) {
+          const int jg = jg0 + j, st = jg & 1;
+          const uint32_t s_col = tmem + (st ? kSCol1 : kSCol0);
+          ok = mbar_wait(&kdeq[st], (uint32_t)((jg >> 1) & 1), err) && ok;  // K(jg) written to buffer st
+          // S[st] is free: the softmax of KV tile jg-2 read it before PV(jg-2) was issued
           if (!ok) break;
           tc_fence_after();
+          const uint32_t kd = st ? dK1 : dK0;  // low descriptor word of K buffer st
 #pragma unroll
-          for (int kk = 4 * hv; kk < 4 * hv + 4; ++kk) {
-            const uint32_t pa = p_col + 8 * kk;  // P columns of keys 16kk..16kk+15
-            const uint32_t boff = (uint32_t)(kk * 16 * 128) >> 4;
-            if (kk == 0) tc_mma_ts_w(tmem + kOCol, pa, dV + boff, dHiV, kIdescPV, jp > 0 ? 1u : 0u);
-            else tc_mma_ts_w<1>(tmem + kOCol, pa, dV + boff, dHiV, kIdescPV);
-            if (L::kVLo) tc_mma_ts_w<1>(tmem + kOCol, pa, dV + (L::kTile >> 4) + boff, dHiV, kIdescPV);
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (uint32_t)((ks >> 2) * (kChunkN * 128) + (ks & 3) * 32) >> 4;
+            if (ks == 0) tc_mma_ts_w<0>(s_col, tmem + kQCol, kd + off, dHiK, kIdescQK);
+            else tc_mma_ts_w<1>(s_col, tmem + kQCol + 8 * ks, kd + off, dHiK, kIdescQK);
+            if (L::kKLo) tc_mma_ts_w<1>(s_col, tmem + kQCol + 8 * ks, kd + (L::kTile >> 4) + off, dHiK, kIdescQK);
           }
-          tc_commit(&pvh_done[hv]);
+          tc_commit(&qk_done[st]);
         }
-        if (!ok) break;
-        tc_commit(&pv_done[sp]);
+        if (j > 0) {
+          const int jp = jg0 + j - 1, sp = jp & 1;
+          ok = mbar_wait(&sm_done[sp], (uint32_t)((jp >> 1) & 1), err) && ok;  // P(jp) written, O rescaled
+          const uint32_t p_col = tmem + kPCol;
+#pragma unroll
+          for (int hv = 0; hv < 2; ++hv) {
+            ok = mbar_wait(&vdeq[hv], (uint32_t)(jp & 1), err) && ok;  // V half hv of KV tile jp written
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 4 * hv; kk < 4 * hv + 4; ++kk) {
+              const uint32_t pa = p_col + 8 * kk;  // P columns of keys 16kk..16kk+15
+              const uint32_t boff = (uint32_t)(kk * 16 * 128) >> 4;
+              // the tile's first PV overwrites O (the softmax group has stored the last tile's)
+              if (kk == 0) tc_mma_ts_w(tmem + kOCol, pa, dV + boff, dHiV, kIdescPV, j > 1 ? 1u : 0u);
+              else tc_mma_ts_w<1>(tmem + kOCol, pa, dV + boff, dHiV, kIdescPV);
+              if (L::kVLo) tc_mma_ts_w<1>(tmem + kOCol, pa, dV + (L::kTile >> 4) + boff, dHiV, kIdescPV);
+            }
+            tc_commit(&pvh_done[hv]);
+          }
+          if (!ok) break;
+          tc_commit(&pv_done[sp]);
+        }
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
       }
-      if (*abort_flag) break;
+      jg0 += n_kv;
     }
     if (!ok) *abort_flag = 1;
     // nothing this thread started may still run when TMEM is released
@@ -1090,15 +1142,15 @@ template <int FK, int FV, int D>
 __global__ void __launch_bounds__(kFusedThreads, 1) mixed_attention_kernel(AttnParams p, unsigned int* err) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tile = blockIdx.x;
-  if (tile < p.n_chunk_tiles) {
-    chunk_tile<FK, FV, D>(p, p.tiles[tile], tile, smem, err);
+  if (tile < p.n_chunk_ctas) {
+    chunk_cta<FK, FV, D>(p, tile, p.n_chunk_ctas, smem, err);
   } else {
     // two decode tiles per CTA where they fit, one on each half of its warps and
     // shared memory; else one on the first half
     using FS = FusedSmem<FK, FV, D>;
     const int half = threadIdx.x >= kThreads ? 1 : 0;
     if (half && !FS::kTwoDecode) return;
-    const int d = FS::kDecodePerCta * (tile - p.n_chunk_tiles) + half;
+    const int d = FS::kDecodePerCta * (tile - p.n_chunk_ctas) + half;
     if (d >= p.n_decode_tiles) return;
     decode_tile<FK, FV, D, FS::kDecodeStages>(p, p.tiles[p.n_chunk_tiles + d], d, smem + half * FS::kHalfBytes, err,
                                               half);
@@ -1112,13 +1164,38 @@ __global__ void __launch_bounds__(kThreads, MINB) decode_attention_kernel(AttnPa
   decode_tile<FK, FV, D, NS>(p, p.tiles[tile], blockIdx.x, smem, err, 0);
 }
 
+// Chunk tiles whose mean KV-tile count is below this are walked by persistent
+// CTAs.
+constexpr int kPersistMaxKvTiles = 64;
+
+// SMs of the current device, read once per device (a very large count when it
+// cannot be read: then every chunk tile gets its own CTA).
+inline int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1 << 30;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1 << 30;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 template <int FK, int FV, int D>
 cudaError_t launch_attention_t(const AttnParams& p, unsigned int* err, cudaStream_t s) {
   using DS = DecodeSmem<FK, FV, D>;
   const int n_tiles = p.n_chunk_tiles + p.n_decode_tiles;
   if (n_tiles == 0) return cudaSuccess;
   constexpr int kPer = FusedSmem<FK, FV, D>::kDecodePerCta;  // decode tiles per fused CTA
-  const int n_fused_ctas = p.n_chunk_tiles + (p.n_decode_tiles + kPer - 1) / kPer;
+  // short chunk tiles run on at most one CTA per SM, each walking several (the
+  // next tile's loads and first MMAs then overlap this tile's last softmax and
+  // its epilogue, ~15k cycles a tile); long ones, where that overlap is worth
+  // little, one per CTA
+  AttnParams q = p;
+  const bool persist = p.n_chunk_tiles > 0 && p.chunk_kv_tiles < kPersistMaxKvTiles * p.n_chunk_tiles;
+  q.n_chunk_ctas = persist ? std::min(p.n_chunk_tiles, sm_count()) : p.n_chunk_tiles;
+  const int n_fused_ctas = q.n_chunk_ctas + (p.n_decode_tiles + kPer - 1) / kPer;
   constexpr int kDec = DS::kTotal;
   constexpr int kFused = FusedSmem<FK, FV, D>::kBytes;
   auto* dec_kernel = decode_attention_kernel<FK, FV, D, DS::kSoloMinBlocks, DS::kSoloStages>;
@@ -1134,7 +1211,7 @@ cudaError_t launch_attention_t(const AttnParams& p, unsigned int* err, cudaStrea
   if (p.n_chunk_tiles == 0) {
     dec_kernel<<<p.n_decode_tiles, kThreads, kDec, s>>>(p, err);
   } else {
-    mixed_attention_kernel<FK, FV, D><<<n_fused_ctas, kFusedThreads, kFused, s>>>(p, err);
+    mixed_attention_kernel<FK, FV, D><<<n_fused_ctas, kFusedThreads, kFused, s>>>(q, err);
   }
   return cudaGetLastError();
 }

@@ -124,6 +124,8 @@ struct AttnParams {
   int32_t max_pages;
   int32_t num_pages;
   int32_t n_chunk_tiles;
+  int32_t n_chunk_ctas;       // CTAs walking the chunk tiles (set by the launcher)
+  int32_t chunk_kv_tiles;     // KV tiles over all chunk tiles
   int32_t n_decode_tiles;
   int32_t hq;
   int32_t hkv;

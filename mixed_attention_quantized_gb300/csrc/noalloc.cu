@@ -86,7 +86,7 @@ int check_cache_noalloc(const mixattn_kv_cache* c) {
 // zeroed split counters.  Returns a status; fills the layout and counts.
 int tile_into_upload(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* kinds, const int32_t* seq,
                      const int32_t* off, int max_pages, WorkspaceLayout* L_out, int* n_chunk_out,
-                     int* n_decode_out) {
+                     int* n_decode_out, int32_t* kv_tiles_out) {
   if (n_rows <= 0 || !kinds || !seq || !off || max_pages <= 0) return MIXATTN_ERR_INVALID_ARG;
   if (hq <= 0 || hq % c.num_kv_heads != 0) return MIXATTN_ERR_INVALID_ARG;
   const int G = hq / c.num_kv_heads;
@@ -125,7 +125,7 @@ int tile_into_upload(const mixattn_kv_cache& c, int hq, int n_rows, const int32_
   memset(g_upload, 0, L.upload_end - L.rows);
   RowInfo* rows = reinterpret_cast<RowInfo*>(g_upload);
   TileDesc* tiles = reinterpret_cast<TileDesc*>(g_upload + (L.tiles - L.rows));
-  int64_t ic = 0, id = n_chunk, q0 = 0;
+  int64_t ic = 0, id = n_chunk, q0 = 0, kv_tiles = 0;
   for (int r = 0; r < n_rows; ++r) {
     const int64_t s = seq[r], o = off[r], nq = s - o;
     const int64_t n_pages = (s + kPage - 1) / kPage;
@@ -138,7 +138,9 @@ int tile_into_upload(const mixattn_kv_cache& c, int hq, int n_rows, const int32_
         for (int64_t b = 0; b < nq; b += T) {
           const int32_t cnt = (int32_t)std::min<int64_t>(T, nq - b);
           const int64_t key_end = std::min<int64_t>(s, o + b + cnt);
-          tiles[ic++] = TileDesc{r, g, (int32_t)b, cnt, 0, (int32_t)((key_end + kChunkN - 1) / kChunkN), 0, 1};
+          const int32_t n_kv = (int32_t)((key_end + kChunkN - 1) / kChunkN);
+          tiles[ic++] = TileDesc{r, g, (int32_t)b, cnt, 0, n_kv, 0, 1};
+          kv_tiles += n_kv;
         }
     } else {
       const int pps = decode_pages_per_split((int)n_pages);
@@ -164,6 +166,7 @@ int tile_into_upload(const mixattn_kv_cache& c, int hq, int n_rows, const int32_
     return a.begin < b.begin;
   });
   *L_out = L;
+  *kv_tiles_out = (int32_t)std::min<int64_t>(kv_tiles, INT32_MAX);
   *n_chunk_out = (int)n_chunk;
   *n_decode_out = (int)n_decode;
   return MIXATTN_OK;
@@ -190,8 +193,9 @@ extern "C" int mixattn_mixed_attention_noalloc(const mixattn_kv_cache* cache, in
   std::lock_guard<std::mutex> lock(g_upload_mu);
   WorkspaceLayout L;
   int n_chunk = 0, n_decode = 0;
+  int32_t chunk_kv_tiles = 0;
   st = tile_into_upload(*cache, num_q_heads, n_rows, row_kinds, seq_lens, q_offsets, max_pages, &L, &n_chunk,
-                        &n_decode);
+                        &n_decode, &chunk_kv_tiles);
   if (st != MIXATTN_OK) return st;
   // pageable source: the call returns once g_upload has been consumed
   if (cudaMemcpyAsync(ws + L.rows, g_upload, L.upload_end - L.rows, cudaMemcpyHostToDevice, s) != cudaSuccess)
@@ -217,6 +221,7 @@ extern "C" int mixattn_mixed_attention_noalloc(const mixattn_kv_cache* cache, in
   p.max_pages = max_pages;
   p.num_pages = cache->num_pages;
   p.n_chunk_tiles = n_chunk;
+  p.chunk_kv_tiles = chunk_kv_tiles;
   p.n_decode_tiles = n_decode;
   p.hq = num_q_heads;
   p.hkv = cache->num_kv_heads;
