@@ -10,13 +10,15 @@
 // Decode tiles (HBM-bound, ~7.5 FLOP per byte): a CTA of 8 warps walks a page
 // range of one (row, kv head).  Each warp keeps several 16-key M-tiles in
 // flight through a cp.async ring in shared memory (16-byte chunks, 128-byte
-// XOR swizzle so the fragment reads are conflict free) and runs QK^T and PV on
-// mma.sync m16n8k16 with the G query heads in the N=8 dimension.  Quantised codes are
-// turned into exact fp16 integers by a byte permute (no rounding); the Q8_0 /
-// Q4_0 scales are applied in fp32: per key and 32-d block on the scores, and
-// folded into P per key and block on the values.  Warp partials are merged in
-// shared memory, split partials by the last CTA of the (row, kv head) to
-// finish (atomic ticket, no spin).
+// XOR swizzle so the ldmatrix reads are conflict free) and runs QK^T and PV on
+// mma.sync m16n8k16 with the G query heads in rows of QK's A and the N=8
+// dimension of PV.  Quantised codes reach the tensor cores as exact fp16
+// subnormals (one or two logic ops per pair of codes, the code offset taken out
+// through the accumulator start and one extra MMA per block); the Q8_0 / Q4_0
+// scales are applied in fp32: per key and 32-d block on the scores, and folded
+// into P per key and block on the values.  Warp partials are merged in shared
+// memory, split partials by the last CTA of the (row, kv head) to finish
+// (atomic ticket, no spin).
 //
 // Chunk tiles (tensor-bound): a CTA of 16 warps owns 128 rows = 128/G query
 // tokens x G heads of one kv head.  Two dequant warp groups load the raw K and V
@@ -63,8 +65,11 @@ struct ChunkSmem {
 // Staging ring of a decode warp: one stage = one M-tile (16 keys) of one page:
 // the 16 contiguous K and V rows of the page plane, copied cooperatively in
 // 16-byte chunks and placed with a 128-byte XOR swizzle (16-byte chunk index ^=
-// 128-byte line index mod 8), so the fragment reads of every format are
-// bank-conflict free; then the 16 keys' K and V scale rows.
+// 128-byte line index mod 8), so every ldmatrix read (8 keys x one 16-byte
+// chunk) hits 8 distinct bank groups; then the 16 keys' raw K and V scale rows.
+// Beside its ring each warp keeps the scales of the M-tile it is working on as
+// fp32, [K | V][block][lane quad c][4]: the quad c = 0..3 holding keys 2c, 2c+1,
+// 2c+8, 2c+9 reads its four scales of one block with one 16-byte load.
 template <int FK, int FV, int D>
 struct DecodeSmem {
   static constexpr int kNb = D / kBlock;
@@ -76,17 +81,33 @@ struct DecodeSmem {
   static constexpr int kKs = kV + 16 * kRbV;
   static constexpr int kVs = kKs + (FK == MIXATTN_KV_F16 ? 0 : kSc);
   static constexpr int kStage = (kVs + (FV == MIXATTN_KV_F16 ? 0 : kSc) + 127) / 128 * 128;
+  // fp32 scales of the current M-tile, per warp: K then V, 16 keys x D/32 blocks each
+  static constexpr int kFsK = FK == MIXATTN_KV_F16 ? 0 : 64 * kNb;
+  static constexpr int kFs = kFsK + (FV == MIXATTN_KV_F16 ? 0 : 64 * kNb);
+  __host__ __device__ static constexpr int kWarpBytes(int ns) { return ns * kStage + kFs; }
+  // after the rings, shared by the tile's warps, [16-byte word j][lane]: the lanes' Q
+  // fragments (D/16 k-steps x 2 words), score-accumulator starts (4 floats) and
+  // one-hot words of the value correction (4)
+  static constexpr int kQBytes = (kNb + 2) * 512;
+  __host__ __device__ static constexpr int q_off(int ns) { return kWarps * kWarpBytes(ns); }
   static constexpr int stages_for(int budget) {
-    return budget / (kWarps * kStage) > 8 ? 8 : (budget / (kWarps * kStage) < 2 ? 2 : budget / (kWarps * kStage));
+    return (budget - kWarps * kFs - kQBytes) / (kWarps * kStage) > 8
+               ? 8
+               : ((budget - kWarps * kFs - kQBytes) / (kWarps * kStage) < 2
+                      ? 2
+                      : (budget - kWarps * kFs - kQBytes) / (kWarps * kStage));
   }
   // after the page loop the same memory holds the warp partials: m[8], l[8], O[8][D]
   static constexpr int kPerWarp = 16 + kMaxGroup * D;
   static constexpr int kMerge = kWarps * kPerWarp * 4;
-  static constexpr int total(int ns) { return (kWarps * ns * kStage > kMerge ? kWarps * ns * kStage : kMerge) + 16; }
-  // decode-only launches: two CTAs per SM when two stages per warp fit in ~106 KB,
-  // else one CTA per SM with a deeper ring
-  static constexpr int kPairBudget = 106 * 1024;
-  static constexpr bool kTwoPerSm = kWarps * 2 * kStage <= kPairBudget;
+  static constexpr int total(int ns) {
+    return (q_off(ns) + kQBytes > kMerge ? q_off(ns) + kQBytes : kMerge) + 16;
+  }
+  // decode-only launches: two CTAs per SM when two stages per warp fit in 113 KB
+  // (half an SM's shared memory less the per-CTA reserve), else one CTA per SM
+  // with a deeper ring
+  static constexpr int kPairBudget = 113 * 1024;
+  static constexpr bool kTwoPerSm = kWarps * kWarpBytes(2) + kQBytes <= kPairBudget;
   static constexpr int kSoloStages = stages_for(kTwoPerSm ? kPairBudget : 212 * 1024);
   static constexpr int kSoloMinBlocks = kTwoPerSm ? 2 : 1;
   static constexpr int kTotal = total(kSoloStages);
@@ -105,34 +126,86 @@ __device__ __forceinline__ constexpr int row_bytes() {
   return F == MIXATTN_KV_F16 ? 2 * D : (F == MIXATTN_KV_Q8_0 ? D : D / 2);
 }
 
-// Physical head dimension d held by lane row `rr` (0..15) of PV M-tile t,
-// for the V format's fragment layout.
+// Four 8x8 b16 matrices from shared memory; the rows of matrix m are the 16-byte
+// rows at the addresses of lanes 8m .. 8m+7.  Lane 4i + j receives elements
+// (i, 2j) and (i, 2j+1) of each matrix; with .trans, elements (2j, i) and
+// (2j+1, i).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// ldmatrix plan of one 16-key M-tile of `RB`-byte rows: its 2 x RB/16 tiles
+// (n-tile nt = keys 8nt..8nt+7, 16-byte chunk ch), tile t = nt * kCh + ch, go
+// four to a load; load L covers tiles 4L .. 4L+3.
+template <int RB>
+struct LdsmPlan {
+  static constexpr int kCh = RB / 16;                     // chunks per key row
+  static constexpr int kGroups = kCh >= 4 ? kCh / 4 : 1;  // loads per n-tile (1 load for both when kCh == 2)
+  static constexpr int kLoads = kCh >= 4 ? kCh / 2 : 1;
+  // the n-tile 1 load of a group sits 8 rows further, the same swizzle phase
+  static constexpr bool kNtAdds = (8 * RB) % 1024 == 0;
+  static constexpr int kOffs = kNtAdds || kCh < 4 ? kGroups : 2 * kGroups;
+  // the lane's row address (offset in the staged region) for load L
+  static __device__ __forceinline__ int lane_off(int L, int lane) {
+    const int t = 4 * L + (lane >> 3);
+    const int nt = t / kCh, ch = t - nt * kCh;
+    return swz((8 * nt + (lane & 7)) * RB + 16 * ch);
+  }
+};
+
+// Words of chunks 4h .. 4h+3 of both n-tiles (kCh == 2: chunks 0, 1 of both,
+// in w0[0..1] and w1[0..1]).
+template <int RB, bool TRANS>
+__device__ __forceinline__ void ldsm_group(uint32_t base, const int (&off)[LdsmPlan<RB>::kOffs], int h,
+                                           uint32_t (&w0)[4], uint32_t (&w1)[4]) {
+  using P = LdsmPlan<RB>;
+  if (P::kCh < 4) {
+    uint32_t r[4];
+    if (TRANS) ldsm_x4_t(base + off[0], r); else ldsm_x4(base + off[0], r);
+    w0[0] = r[0]; w0[1] = r[1]; w1[0] = r[2]; w1[1] = r[3];
+    w0[2] = w0[3] = w1[2] = w1[3] = 0u;
+  } else {
+    const uint32_t a0 = base + off[h];
+    const uint32_t a1 = P::kNtAdds ? a0 + 8 * RB : base + off[P::kGroups + h];
+    if (TRANS) { ldsm_x4_t(a0, w0); ldsm_x4_t(a1, w1); } else { ldsm_x4(a0, w0); ldsm_x4(a1, w1); }
+  }
+}
+
+// Quantised codes -> fp16 subnormals: the 16-bit pattern holding a small
+// unsigned integer u (< 1024) is the fp16 number u * 2^-24, exactly.
+//   Q8_0: bytes 0 and 2 (even) or 1 and 3 (odd) of a word, sign bit flipped:
+//         u = q + 128
+//   Q4_0: low (u = n) or high (u = 16 n) nibble of bytes 0 and 2 (even) or 1 and 3 (odd)
+__device__ __forceinline__ uint32_t q8_even(uint32_t w) { return (w ^ 0x80808080u) & 0x00FF00FFu; }
+__device__ __forceinline__ uint32_t q8_odd(uint32_t w) { return ((w >> 8) ^ 0x00800080u) & 0x00FF00FFu; }
+__device__ __forceinline__ uint32_t q4_lo_even(uint32_t w) { return w & 0x000F000Fu; }
+__device__ __forceinline__ uint32_t q4_lo_odd(uint32_t w) { return (w >> 8) & 0x000F000Fu; }
+__device__ __forceinline__ uint32_t q4_hi_even(uint32_t w) { return w & 0x00F000F0u; }
+__device__ __forceinline__ uint32_t q4_hi_odd(uint32_t w) { return (w >> 8) & 0x00F000F0u; }
+
+// Code offset of a format as an fp16 subnormal pair, negated: -128 * 2^-24
+// (Q8_0) or -8 * 2^-24 (Q4_0).
+template <int F>
+__device__ __forceinline__ constexpr uint32_t neg_offset_pair() {
+  return F == MIXATTN_KV_Q8_0 ? 0x80808080u : 0x80088008u;
+}
+
+// Head dimension held by row `rr` (0..15) of PV M-tile t.
+//   quantised V: 32-d block t/2, half t%2, element 2(rr%8) + rr/8 of the half
+//   fp16 V:      16t + rr
 template <int FV>
 __device__ __forceinline__ int pv_row_to_d(int t, int rr) {
-  const int b = t >> 1, u = t & 1, r = rr & 7, hi = rr >> 3;
-  if (FV == MIXATTN_KV_Q4_0) return 32 * b + 16 * u + 2 * r + hi;
-  return 32 * b + 4 * r + 2 * u + hi;
-}
-
-__device__ __forceinline__ void unpack_scales(uint2 a, float* out) {
-  out[0] = __half2float(__ushort_as_half(a.x & 0xFFFF));
-  out[1] = __half2float(__ushort_as_half(a.x >> 16));
-  out[2] = __half2float(__ushort_as_half(a.y & 0xFFFF));
-  out[3] = __half2float(__ushort_as_half(a.y >> 16));
-}
-
-template <int NB>
-__device__ __forceinline__ void load_scales(const uint8_t* p, float (&out)[NB]) {
-  if (NB == 4) {
-    float t[4];
-    unpack_scales(lds64(p), t);
-#pragma unroll
-    for (int i = 0; i < NB; ++i) out[i] = t[i];
-  } else {
-    const uint32_t a = lds32(p);
-    out[0] = __half2float(__ushort_as_half(a & 0xFFFF));
-    out[NB - 1] = __half2float(__ushort_as_half(a >> 16));
-  }
+  if (FV == MIXATTN_KV_F16) return 16 * t + rr;
+  return 16 * t + 2 * (rr & 7) + (rr >> 3);
 }
 
 // Barrier over the 8 warps of a decode tile (a fused-launch CTA runs one tile
@@ -141,6 +214,24 @@ __device__ __forceinline__ void decode_sync(int half) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + half), "n"(kThreads) : "memory");
 }
 
+__device__ __forceinline__ float h2f_lo(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x & 0xFFFFu))); }
+__device__ __forceinline__ float h2f_hi(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x >> 16))); }
+
+// One decode tile: a page range of one (row, kv head), 8 warps, each warp
+// walking its own pages 16 keys (one M-tile) at a time.
+//
+// Quantised K and V reach the tensor cores as fp16 subnormals: the 16-bit
+// pattern of a small unsigned integer u is the fp16 number u * 2^-24 exactly,
+// so one or two logic ops per pair of codes make an exact operand (Q8_0:
+// u = q + 128; Q4_0: u = n, or 16 n for the high nibble, which the matching Q
+// entries take as q / 16 or the epilogue divides out).  The code offset is
+// taken out exactly where it is cheapest:
+//   scores: the block's accumulator starts at -offset * sum(q over the block) * 2^-24,
+//           so the MMA ends on sum q * (u - offset) * 2^-24;
+//   values: O += V_u^T P' per block, and one more MMA per block with a one-hot
+//           A row of -offset * 2^-24 sums the same fp16 P' into row b of `corr`,
+//           added to the block's rows at the end.
+// The 2^24 is folded into the softmax scale (scores) and the epilogue (values).
 template <int FK, int FV, int D, int NS>
 __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc& t, int dec_idx, uint8_t* smem,
                                             unsigned int* err, int half) {
@@ -149,6 +240,12 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   constexpr int KS = D / 16;       // k-steps of QK / M-tiles of PV
   constexpr int RBK = row_bytes<FK, D>();
   constexpr int RBV = row_bytes<FV, D>();
+  constexpr bool QK = FK != MIXATTN_KV_F16;
+  constexpr bool QV = FV != MIXATTN_KV_F16;
+  using PK = LdsmPlan<RBK>;
+  using PV = LdsmPlan<RBV>;
+  constexpr float kTwo24 = 16777216.f;
+  constexpr float kTwoM24 = 5.9604644775390625e-8f;
 
   // `half`: which 8 warps of the CTA run this tile (a fused-launch CTA runs two)
   const int tid = threadIdx.x - half * kThreads, warp = tid >> 5, lane = tid & 31;
@@ -165,162 +262,246 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   const int n_mt = wp1 > wp0 ? 2 * (wp1 - wp0) : 0;  // the warp's M-tiles (16 keys each)
 
   // ---- Q as the A operand of S = Q K^T: head r in M row r (rows 8..15 zero) ----
-  // k-slots 2c,2c+1 | 2c+8,2c+9 of k-step 2b+hs hold head dims
-  //   Q8_0 / fp16: 32b+8c+4hs + {0,1 | 2,3};   Q4_0: 32b+16hs+4c + {0,1 | 2,3}
-  uint32_t qa[KS][2];
-  {
+  // quantised K: k-step 2b+j covers dims 32b + 16j + 4c + {0, 2} (a0) and {1, 3}
+  //   (a2), the order of the subnormal pairs of one K word; for Q4_0 the j = 1
+  //   k-step (high nibbles, 16 n) takes q / 16
+  // fp16 K: k-step ks covers dims 16ks + 2c + {0, 1} (a0) and {8, 9} (a2)
+  // written once by warp 0 into the tile's Q block: word j (j < NB) of a lane holds the
+  // fragments of k-steps 2j, 2j+1 (a0, a2 each), word NB the four block starts, word
+  // NB + 1 the one-hot words of the value correction
+  const uint32_t q_s = smem_u32(smem) + S::q_off(NS);
+  if (warp == 0) {
+    uint32_t qa[KS][2];
+    float cb[4] = {0.f, 0.f, 0.f, 0.f};  // start of block b's score accumulator (head r)
     const bool real = r < G;
     const uint16_t* qrow =
         static_cast<const uint16_t*>(p.q) + ((int64_t)ri.q_start * p.hq + (int64_t)g * G + (real ? r : 0)) * D;
+    if (!QK) {
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      if (FK == MIXATTN_KV_Q4_0) {
-        uint2 lo = real ? ldg_u64(qrow + 32 * b + 4 * c) : make_uint2(0u, 0u);
-        uint2 hi = real ? ldg_u64(qrow + 32 * b + 16 + 4 * c) : make_uint2(0u, 0u);
-        qa[2 * b][0] = lo.x;
-        qa[2 * b][1] = lo.y;
-        qa[2 * b + 1][0] = hi.x;
-        qa[2 * b + 1][1] = hi.y;
-      } else {
-        uint4 v = real ? ldg_u128(qrow + 32 * b + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
-        qa[2 * b][0] = v.x;
-        qa[2 * b][1] = v.y;
-        qa[2 * b + 1][0] = v.z;
-        qa[2 * b + 1][1] = v.w;
+      for (int ks = 0; ks < KS; ++ks) {
+        qa[ks][0] = real ? ldg_u32(qrow + 16 * ks + 2 * c) : 0u;
+        qa[ks][1] = real ? ldg_u32(qrow + 16 * ks + 8 + 2 * c) : 0u;
+      }
+    } else {
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        float qs = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          uint2 v = ldg_u64(qrow + 32 * b + 16 * j + 4 * c);
+          if (!real) v = make_uint2(0u, 0u);
+          qs += (h2f_lo(v.x) + h2f_hi(v.x)) + (h2f_lo(v.y) + h2f_hi(v.y));
+          uint32_t e = prmt(v.x, v.y, 0x5410u), o = prmt(v.x, v.y, 0x7632u);
+          if (FK == MIXATTN_KV_Q4_0 && j == 1) {
+            e = hmul2_u32(e, 0x2C002C00u);  // x 1/16
+            o = hmul2_u32(o, 0x2C002C00u);
+          }
+          qa[2 * b + j][0] = e;
+          qa[2 * b + j][1] = o;
+        }
+        qs += __shfl_xor_sync(0xFFFFFFFFu, qs, 1);
+        qs += __shfl_xor_sync(0xFFFFFFFFu, qs, 2);
+        cb[b] = qs * (FK == MIXATTN_KV_Q8_0 ? -128.f : -8.f) * kTwoM24;
       }
     }
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+      sts128_s(q_s + 512 * j + 16 * lane, make_uint4(qa[2 * j][0], qa[2 * j][1], qa[2 * j + 1][0], qa[2 * j + 1][1]));
+    sts128_s(q_s + 512 * NB + 16 * lane,
+             make_uint4(__float_as_uint(cb[0]), __float_as_uint(cb[1]), __float_as_uint(cb[2]), __float_as_uint(cb[3])));
+    const uint32_t off = neg_offset_pair<FV>();
+    sts128_s(q_s + 512 * (NB + 1) + 16 * lane,
+             make_uint4(r == 0 ? off : 0u, r == 1 ? off : 0u, r == 2 ? off : 0u, r == 3 ? off : 0u));
   }
+  decode_sync(half);
 
   float o_acc[KS][4];
 #pragma unroll
   for (int i = 0; i < KS; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
-  float m_run = -CUDART_INF_F, l_run = 0.f;  // head r
-  const float sl2 = p.scale_log2;
+  float corr[4] = {0.f, 0.f, 0.f, 0.f};  // quantised V: row b, heads 2c, 2c+1
+  float m_run = -CUDART_INF_F, l_run = 0.f;  // head r, in log2 units
+  const float sl2 = QK ? p.scale_log2 * kTwo24 : p.scale_log2;
 
-  const uint8_t* kq_base = p.k_quant + (int64_t)g * kPage * RBK;
-  const uint8_t* vq_base = p.v_quant + (int64_t)g * kPage * RBV;
-  const uint8_t* ks_base = reinterpret_cast<const uint8_t*>(p.k_scale) + (int64_t)g * kPage * NB * 2;
-  const uint8_t* vs_base = reinterpret_cast<const uint8_t*>(p.v_scale) + (int64_t)g * kPage * NB * 2;
-  const int64_t kq_page_stride = (int64_t)p.hkv * kPage * RBK;
-  const int64_t vq_page_stride = (int64_t)p.hkv * kPage * RBV;
-  const int64_t sc_page_stride = (int64_t)p.hkv * kPage * NB * 2;
   const int32_t* pt_row = p.page_table + (int64_t)t.row * p.max_pages;
-  uint8_t* ring = smem + warp * NS * S::kStage;
+  const uint32_t ring_s = smem_u32(smem) + warp * S::kWarpBytes(NS);
+  const uint32_t fs_s = ring_s + NS * S::kStage;  // fp32 scales of the current M-tile
+  int offk[PK::kOffs], offv[PV::kOffs];
+#pragma unroll
+  for (int i = 0; i < PK::kOffs; ++i) offk[i] = PK::lane_off(i, lane);
+#pragma unroll
+  for (int i = 0; i < PV::kOffs; ++i) offv[i] = PV::lane_off(i, lane);
+  // cp.async destinations: chunk lane + 32k of a region sits at cpo[k & 1] + 512 (k & ~1)
+  // (the swizzle repeats every 1024 bytes)
+  const int cpo0 = swz(16 * lane), cpo1 = swz(16 * lane + 512);
+
+  // The warp's page ids, lane j holding page wp0 + j (at most 32 a warp); a page
+  // outside the cache is flagged once and skipped.
+  const int n_pg = wp1 > wp0 ? wp1 - wp0 : 0;
+  int my_pid = lane < n_pg ? pt_row[wp0 + lane] : 0;
+  const bool pid_ok = my_pid >= 0 && my_pid < p.num_pages;
+  const uint32_t page_ok = __ballot_sync(0xFFFFFFFFu, pid_ok);
+  if (lane < n_pg && !pid_ok) set_device_error(err, MIXATTN_DEVERR_PAGE_ID);
 
   // Issue the copies of the warp's M-tile i into its stage, then close the group
   // (an empty group for i past the end keeps the group count uniform).
+  int st_issue = 0;  // ring stage of the next M-tile to issue (M-tile i -> stage i % NS)
   auto issue = [&](int i) {
     if (i < n_mt) {
-      const int pg = wp0 + (i >> 1), mt = i & 1;
-      const int pid = pt_row[pg];
-      if (pid >= 0 && pid < p.num_pages) {
-        uint8_t* st = ring + (i % NS) * S::kStage;
-        const uint8_t* kq = kq_base + (int64_t)pid * kq_page_stride + 16 * mt * RBK;
-        const uint8_t* vq = vq_base + (int64_t)pid * vq_page_stride + 16 * mt * RBV;
+      const int mt = i & 1;
+      const int pid = __shfl_sync(0xFFFFFFFFu, my_pid, i >> 1);
+      if ((page_ok >> (i >> 1)) & 1u) {
+        const uint32_t st = ring_s + st_issue * S::kStage;
+        const int64_t prow = (int64_t)pid * p.hkv + g;  // (page, kv head) plane
+        const uint8_t* kq = p.k_quant + prow * (kPage * RBK) + (16 * mt * RBK + 16 * lane);
+        const uint8_t* vq = p.v_quant + prow * (kPage * RBV) + (16 * mt * RBV + 16 * lane);
 #pragma unroll
-        for (int j = lane; j < RBK; j += 32) cp_async16(st + S::kK + swz(16 * j), kq + 16 * j);
+        for (int k = 0; k < RBK / 32; ++k)
+          cp_async16_s(st + S::kK + ((k & 1) ? cpo1 : cpo0) + 512 * (k & ~1), kq + 512 * k);
 #pragma unroll
-        for (int j = lane; j < RBV; j += 32) cp_async16(st + S::kV + swz(16 * j), vq + 16 * j);
+        for (int k = 0; k < RBV / 32; ++k)
+          cp_async16_s(st + S::kV + ((k & 1) ? cpo1 : cpo0) + 512 * (k & ~1), vq + 512 * k);
         constexpr int SC = S::kSc / 16;  // 16-byte chunks of one scale slice
+        const int64_t so = prow * (kPage * NB * 2) + 16 * mt * NB * 2;
         if (FK != MIXATTN_KV_F16 && lane < SC)
-          cp_async16(st + S::kKs + 16 * lane, ks_base + (int64_t)pid * sc_page_stride + 16 * mt * NB * 2 + 16 * lane);
+          cp_async16_s(st + S::kKs + 16 * lane, reinterpret_cast<const uint8_t*>(p.k_scale) + so + 16 * lane);
         if (FV != MIXATTN_KV_F16 && lane >= 16 && lane < 16 + SC)
-          cp_async16(st + S::kVs + 16 * (lane - 16),
-                     vs_base + (int64_t)pid * sc_page_stride + 16 * mt * NB * 2 + 16 * (lane - 16));
-      } else if (lane == 0 && (i & 1) == 0) {
-        set_device_error(err, MIXATTN_DEVERR_PAGE_ID);
+          cp_async16_s(st + S::kVs + 16 * (lane - 16),
+                       reinterpret_cast<const uint8_t*>(p.v_scale) + so + 16 * (lane - 16));
       }
     }
     cp_async_commit();
+    st_issue = st_issue + 1 == NS ? 0 : st_issue + 1;
   };
 
 #pragma unroll
   for (int i = 0; i < NS - 1; ++i) issue(i);
 
+  // scale conversion: lanes 0-15 take the K scales of key lane, lanes 16-31 the V scales
+  // of key lane - 16, into slot (key & 1) + 2 (key >> 3) of quad (key & 7) / 2
+  const bool sc_lane = lane >= 16 ? QV : QK;
+  const int sc_src = (lane >= 16 ? S::kVs : S::kKs) + (lane & 15) * NB * 2;
+  const uint32_t sc_dst =
+      fs_s + (lane >= 16 ? S::kFsK : 0) + 4 * ((((lane & 7) >> 1) << 2) + (lane & 1) + (((lane >> 3) & 1) << 1));
   const int kv0 = 2 * c;  // the lane's keys in an M-tile: kv0, kv0+1 (n-tile 0), kv0+8, kv0+9 (n-tile 1)
+  int st_cons = 0;
   for (int i = 0; i < n_mt; ++i) {
     issue(i + NS - 1);        // refills the stage consumed in the previous step
     cp_async_wait<NS - 1>();  // this lane's copies of M-tile i have landed
     __syncwarp();             // ... and every other lane's
-    const int pg = wp0 + (i >> 1), mt = i & 1;
-    const int pid = pt_row[pg];
-    if (pid >= 0 && pid < p.num_pages) {
-      const uint8_t* st = ring + (i % NS) * S::kStage;
-      const int key0 = pg * kPage + 16 * mt;  // first key of the M-tile
+    const uint32_t st_s = ring_s + st_cons * S::kStage;
+    st_cons = st_cons + 1 == NS ? 0 : st_cons + 1;
+    if ((page_ok >> (i >> 1)) & 1u) {
+      const int key0 = (wp0 + (i >> 1)) * kPage + 16 * (i & 1);  // first key of the M-tile
       const bool partial = key0 + 16 > ri.seq_len;
 
-      // ---------------- S = Q K^T: head r x keys kv0, kv0+1, kv0+8, kv0+9 ----------------
-      float s[4] = {0.f, 0.f, 0.f, 0.f};
-      float dk0[NB], dk1[NB], dk8[NB], dk9[NB];
-      if (FK != MIXATTN_KV_F16) {
-        load_scales<NB>(st + S::kKs + kv0 * NB * 2, dk0);
-        load_scales<NB>(st + S::kKs + (kv0 + 1) * NB * 2, dk1);
-        load_scales<NB>(st + S::kKs + (kv0 + 8) * NB * 2, dk8);
-        load_scales<NB>(st + S::kKs + (kv0 + 9) * NB * 2, dk9);
+      // ---------------- scales of the M-tile -> fp32, one key per lane ----------------
+      if (QK || QV) {
+        if (sc_lane) {
+          const uint32_t src = st_s + sc_src;
+          const uint32_t dst = sc_dst;
+          if (NB == 4) {
+            const uint2 x = lds64_s(src);
+            sts32f_s(dst, h2f_lo(x.x));
+            sts32f_s(dst + 64, h2f_hi(x.x));
+            sts32f_s(dst + 128, h2f_lo(x.y));
+            sts32f_s(dst + 192, h2f_hi(x.y));
+          } else {
+            const uint32_t x = lds32_s(src);
+            sts32f_s(dst, h2f_lo(x));
+            sts32f_s(dst + 64, h2f_hi(x));
+          }
+        }
+        __syncwarp();
       }
+
+      // ---------------- S = Q K^T: head r x keys kv0, kv0+1 (s01), kv0+8, kv0+9 (s89) ----------------
+      uint64_t s01, s89;
+      if (QK) {
+        s01 = s89 = 0ull;
+        const float4 cbv = lds128f_s(q_s + 512 * NB + 16 * lane);
+        // blocks per ldmatrix group: Q8_0 two chunks a block, Q4_0 one
+        constexpr int BPG = FK == MIXATTN_KV_Q8_0 ? 2 : (NB < 4 ? NB : 4);
 #pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        const uint8_t* kd = st + S::kK;
-        uint32_t b0[2][2], b1[2][2];  // B fragments [n-tile][reg] of k-steps 2b and 2b+1 (keys r, r+8)
-        if (FK == MIXATTN_KV_Q8_0) {
-          const uint2 wl = lds64(kd + swz(r * RBK + 32 * b + 8 * c));
-          const uint2 wh = lds64(kd + swz((r + 8) * RBK + 32 * b + 8 * c));
-          s8x4_to_f16x2x2(wl.x, b0[0][0], b0[0][1]);
-          s8x4_to_f16x2x2(wh.x, b0[1][0], b0[1][1]);
-          s8x4_to_f16x2x2(wl.y, b1[0][0], b1[0][1]);
-          s8x4_to_f16x2x2(wh.y, b1[1][0], b1[1][1]);
-        } else if (FK == MIXATTN_KV_Q4_0) {
-          const uint32_t yl = lds32(kd + swz(r * RBK + 16 * b + 4 * c));
-          const uint32_t yh = lds32(kd + swz((r + 8) * RBK + 16 * b + 4 * c));
-          u4x4_to_f16x2x2(yl & 0x0F0F0F0Fu, b0[0][0], b0[0][1]);
-          u4x4_to_f16x2x2(yh & 0x0F0F0F0Fu, b0[1][0], b0[1][1]);
-          u4x4_to_f16x2x2((yl >> 4) & 0x0F0F0F0Fu, b1[0][0], b1[0][1]);
-          u4x4_to_f16x2x2((yh >> 4) & 0x0F0F0F0Fu, b1[1][0], b1[1][1]);
-        } else {
-          const uint4 wl = lds128(kd + swz(r * RBK + 2 * (32 * b + 8 * c)));
-          const uint4 wh = lds128(kd + swz((r + 8) * RBK + 2 * (32 * b + 8 * c)));
-          b0[0][0] = wl.x; b0[0][1] = wl.y; b0[1][0] = wh.x; b0[1][1] = wh.y;
-          b1[0][0] = wl.z; b1[0][1] = wl.w; b1[1][0] = wh.z; b1[1][1] = wh.w;
+        for (int h = 0; h < PK::kGroups; ++h) {
+          uint32_t w0[4], w1[4];  // K words of n-tiles 0 and 1 (keys r and r+8)
+          ldsm_group<RBK, false>(st_s + S::kK, offk, h, w0, w1);
+#pragma unroll
+          for (int bb = 0; bb < BPG; ++bb) {
+            const int b = h * BPG + bb;
+            uint32_t k0[2][2], k1[2][2];  // [k-step 2b+j][b0, b1]
+            if (FK == MIXATTN_KV_Q8_0) {
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                k0[j][0] = q8_even(w0[2 * bb + j]);
+                k0[j][1] = q8_odd(w0[2 * bb + j]);
+                k1[j][0] = q8_even(w1[2 * bb + j]);
+                k1[j][1] = q8_odd(w1[2 * bb + j]);
+              }
+            } else {
+              k0[0][0] = q4_lo_even(w0[bb]);
+              k0[0][1] = q4_lo_odd(w0[bb]);
+              k0[1][0] = q4_hi_even(w0[bb]);
+              k0[1][1] = q4_hi_odd(w0[bb]);
+              k1[0][0] = q4_lo_even(w1[bb]);
+              k1[0][1] = q4_lo_odd(w1[bb]);
+              k1[1][0] = q4_hi_even(w1[bb]);
+              k1[1][1] = q4_hi_odd(w1[bb]);
+            }
+            const uint4 qv = lds128_s(q_s + 512 * b + 16 * lane);
+            const float cbb = (b == 0 ? cbv.x : (b == 1 ? cbv.y : (b == 2 ? cbv.z : cbv.w)));
+            const uint32_t a0[4] = {qv.x, 0u, qv.y, 0u};
+            const uint32_t a1[4] = {qv.z, 0u, qv.w, 0u};
+            float u0[4], u1[4];  // sum q (u - offset) 2^-24 over the block, keys kv0.. | kv0+8..
+            mma_16816_c(u0, a0, k0[0], cbb, cbb, 0.f, 0.f);
+            mma_16816(u0, a1, k0[1]);
+            mma_16816_c(u1, a0, k1[0], cbb, cbb, 0.f, 0.f);
+            mma_16816(u1, a1, k1[1]);
+            const float4 dk = lds128f_s(fs_s + b * 64 + c * 16);
+            s01 = ffma2(f2_pack(dk.x, dk.y), f2_pack(u0[0], u0[1]), s01);
+            s89 = ffma2(f2_pack(dk.z, dk.w), f2_pack(u1[0], u1[1]), s89);
+          }
         }
-        const uint32_t a0[4] = {qa[2 * b][0], 0u, qa[2 * b][1], 0u};
-        const uint32_t a1[4] = {qa[2 * b + 1][0], 0u, qa[2 * b + 1][1], 0u};
-        if (FK == MIXATTN_KV_F16) {
-          float u0[4], u1[4];
-          mma_16816_c(u0, a0, b0[0], s[0], s[1], 0.f, 0.f);
-          mma_16816(u0, a1, b1[0]);
-          mma_16816_c(u1, a0, b0[1], s[2], s[3], 0.f, 0.f);
-          mma_16816(u1, a1, b1[1]);
-          s[0] = u0[0]; s[1] = u0[1]; s[2] = u1[0]; s[3] = u1[1];
-        } else {
-          float u0[4], u1[4];  // per-block dot products of exact integer codes
-          mma_16816_c(u0, a0, b0[0], 0.f, 0.f, 0.f, 0.f);
-          mma_16816(u0, a1, b1[0]);
-          mma_16816_c(u1, a0, b0[1], 0.f, 0.f, 0.f, 0.f);
-          mma_16816(u1, a1, b1[1]);
-          s[0] = fmaf(dk0[b], u0[0], s[0]);
-          s[1] = fmaf(dk1[b], u0[1], s[1]);
-          s[2] = fmaf(dk8[b], u1[0], s[2]);
-          s[3] = fmaf(dk9[b], u1[1], s[3]);
+      } else {
+        float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int h = 0; h < PK::kGroups; ++h) {
+          uint32_t w0[4], w1[4];  // chunks 4h .. 4h+3 = k-steps 2h, 2h+1
+          ldsm_group<RBK, false>(st_s + S::kK, offk, h, w0, w1);
+          const uint4 qv = lds128_s(q_s + 512 * h + 16 * lane);  // k-steps 2h, 2h+1
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t a[4] = {j ? qv.z : qv.x, 0u, j ? qv.w : qv.y, 0u};
+            const uint32_t b0[2] = {w0[2 * j], w0[2 * j + 1]};
+            const uint32_t b1[2] = {w1[2 * j], w1[2 * j + 1]};
+            mma_16816(u0, a, b0);
+            mma_16816(u1, a, b1);
+          }
         }
+        s01 = f2_pack(u0[0], u0[1]);
+        s89 = f2_pack(u1[0], u1[1]);
       }
 
       // ---------------- online softmax over the 16 keys (head r) ----------------
-      s[0] = key0 + kv0 < ri.seq_len ? s[0] * sl2 : -CUDART_INF_F;
-      s[1] = key0 + kv0 + 1 < ri.seq_len ? s[1] * sl2 : -CUDART_INF_F;
-      s[2] = key0 + kv0 + 8 < ri.seq_len ? s[2] * sl2 : -CUDART_INF_F;
-      s[3] = key0 + kv0 + 9 < ri.seq_len ? s[3] * sl2 : -CUDART_INF_F;
-      float pm = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+      float s[4];
+      f2_unpack(s01, s[0], s[1]);
+      f2_unpack(s89, s[2], s[3]);
+      if (partial) {
+        s[0] = key0 + kv0 < ri.seq_len ? s[0] : -CUDART_INF_F;
+        s[1] = key0 + kv0 + 1 < ri.seq_len ? s[1] : -CUDART_INF_F;
+        s[2] = key0 + kv0 + 8 < ri.seq_len ? s[2] : -CUDART_INF_F;
+        s[3] = key0 + kv0 + 9 < ri.seq_len ? s[3] : -CUDART_INF_F;
+      }
+      float pm = fmax3(s[0], s[1], fmaxf(s[2], s[3]));
       pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 1));
       pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 2));
-      // exact running max: the largest weight is exactly 1, so its fp16 P' is exact
-      float alpha = 1.f;
-      if (pm > m_run) {  // also the first M-tile with a valid key (m_run = -inf)
-        alpha = ex2(m_run - pm);
-        m_run = pm;
-      }
+      pm *= sl2;  // scale > 0: the maximum of the scaled scores
+      // the running maximum only grows; alpha = 1 exactly when it stays (also -inf -> -inf)
+      const float m_new = fmaxf(m_run, pm);
+      const float alpha = m_new == m_run ? 1.f : ex2(m_run - m_new);
+      m_run = m_new;
       const float mref = m_run == -CUDART_INF_F ? 0.f : m_run;
-      const float p0 = ex2(s[0] - mref), p1 = ex2(s[1] - mref);
-      const float p8 = ex2(s[2] - mref), p9 = ex2(s[3] - mref);
+      const float p0 = ex2(fmaf(s[0], sl2, -mref)), p1 = ex2(fmaf(s[1], sl2, -mref));
+      const float p8 = ex2(fmaf(s[2], sl2, -mref)), p9 = ex2(fmaf(s[3], sl2, -mref));
       l_run = l_run * alpha + ((p0 + p1) + (p8 + p9));
       if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
         // O columns are heads 2c, 2c+1: their factors live in lanes 8c and 8c+4
@@ -333,90 +514,100 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
           o_acc[i2][2] *= a_even;
           o_acc[i2][3] *= a_odd;
         }
+        corr[0] *= a_even;
+        corr[1] *= a_odd;
       }
 
-      // ---------------- O^T += V^T P for the 16 keys ----------------
-      // P is already in the B-operand layout: this lane holds P[key kv0.., kv0+9][head r].
-      uint32_t bfr[NB][2];
-      if (FV == MIXATTN_KV_F16) {
-        bfr[0][0] = pack_f16x2(p0, p1);
-        bfr[0][1] = pack_f16x2(p8, p9);
+      // ---------------- O^T += V^T P' for the 16 keys ----------------
+      // P is already in the B-operand layout: this lane holds P[key kv0.., kv0+9][head r];
+      // quantised V takes P' = P x (the key's scale of the block) per block.
+      uint32_t bq[QV ? NB : 1][2];
+      if (QV) {
+        const uint4 ohv = lds128_s(q_s + 512 * (NB + 1) + 16 * lane);  // one-hot rows of corr
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const float4 dv = lds128f_s(fs_s + S::kFsK + b * 64 + c * 16);
+          float x0, x1, x8, x9;
+          f2_unpack(fmul2(f2_pack(p0, p1), f2_pack(dv.x, dv.y)), x0, x1);
+          f2_unpack(fmul2(f2_pack(p8, p9), f2_pack(dv.z, dv.w)), x8, x9);
+          if (partial) {  // p == 0 (a key past the row) stays 0 whatever its scale slot holds
+            x0 = p0 != 0.f ? x0 : 0.f;
+            x1 = p1 != 0.f ? x1 : 0.f;
+            x8 = p8 != 0.f ? x8 : 0.f;
+            x9 = p9 != 0.f ? x9 : 0.f;
+          }
+          bq[b][0] = pack_f16x2(x0, x1);
+          bq[b][1] = pack_f16x2(x8, x9);
+          // row b of corr += (-offset 2^-24) x sum over the keys of this fp16 P'
+          const uint32_t oh = b == 0 ? ohv.x : (b == 1 ? ohv.y : (b == 2 ? ohv.z : ohv.w));
+          const uint32_t ao[4] = {oh, 0u, oh, 0u};
+          mma_16816(corr, ao, bq[b]);
+        }
       } else {
-        float dv0[NB], dv1[NB], dv8[NB], dv9[NB];
-        load_scales<NB>(st + S::kVs + kv0 * NB * 2, dv0);
-        load_scales<NB>(st + S::kVs + (kv0 + 1) * NB * 2, dv1);
-        load_scales<NB>(st + S::kVs + (kv0 + 8) * NB * 2, dv8);
-        load_scales<NB>(st + S::kVs + (kv0 + 9) * NB * 2, dv9);
-        if (partial) {
-          // p == 0 (a key past the row) stays 0 whatever its scale slot holds
-#pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            bfr[b][0] = pack_f16x2(p0 != 0.f ? p0 * dv0[b] : 0.f, p1 != 0.f ? p1 * dv1[b] : 0.f);
-            bfr[b][1] = pack_f16x2(p8 != 0.f ? p8 * dv8[b] : 0.f, p9 != 0.f ? p9 * dv9[b] : 0.f);
-          }
-        } else {
-#pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            bfr[b][0] = pack_f16x2(p0 * dv0[b], p1 * dv1[b]);
-            bfr[b][1] = pack_f16x2(p8 * dv8[b], p9 * dv9[b]);
-          }
-        }
+        bq[0][0] = pack_f16x2(p0, p1);
+        bq[0][1] = pack_f16x2(p8, p9);
       }
 
 #pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        const uint8_t* vd = st + S::kV;
-        uint32_t a_u0[4], a_u1[4];  // A fragments of PV M-tiles 2b (u=0) and 2b+1 (u=1)
-        const uint32_t* bb = (FV == MIXATTN_KV_F16) ? bfr[0] : bfr[b];
+      for (int h = 0; h < PV::kGroups; ++h) {
+        uint32_t w0[4], w1[4];  // transposed V words of n-tiles 0 and 1: keys (kv0, kv0+1) | (kv0+8, kv0+9)
+        ldsm_group<RBV, true>(st_s + S::kV, offv, h, w0, w1);
         if (FV == MIXATTN_KV_Q8_0) {
-          uint4 w;
-          w.x = lds32(vd + swz(kv0 * RBV + 32 * b + 4 * r));
-          w.y = lds32(vd + swz((kv0 + 1) * RBV + 32 * b + 4 * r));
-          w.z = lds32(vd + swz((kv0 + 8) * RBV + 32 * b + 4 * r));
-          w.w = lds32(vd + swz((kv0 + 9) * RBV + 32 * b + 4 * r));
-          s8x4_to_f16x2x2(prmt(w.x, w.y, 0x5140u), a_u0[0], a_u0[1]);
-          s8x4_to_f16x2x2(prmt(w.z, w.w, 0x5140u), a_u0[2], a_u0[3]);
-          s8x4_to_f16x2x2(prmt(w.x, w.y, 0x7362u), a_u1[0], a_u1[1]);
-          s8x4_to_f16x2x2(prmt(w.z, w.w, 0x7362u), a_u1[2], a_u1[3]);
+          // chunk 4h+m is M-tile 4h+m: rows r, r+8 = its bytes 2r, 2r+1
+          constexpr int MT = PV::kCh < 4 ? PV::kCh : 4;
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const int tt = 4 * h + m;
+            const uint32_t a[4] = {q8_even(w0[m]), q8_odd(w0[m]), q8_even(w1[m]), q8_odd(w1[m])};
+            mma_16816(o_acc[tt], a, bq[tt >> 1]);
+          }
         } else if (FV == MIXATTN_KV_Q4_0) {
-          // the 4 bytes holding the lane's 2 bytes (block bytes 2r, 2r+1) at half (r & 1)
-          uint4 w;
-          w.x = lds32(vd + swz(kv0 * RBV + 16 * b + 4 * (r >> 1)));
-          w.y = lds32(vd + swz((kv0 + 1) * RBV + 16 * b + 4 * (r >> 1)));
-          w.z = lds32(vd + swz((kv0 + 8) * RBV + 16 * b + 4 * (r >> 1)));
-          w.w = lds32(vd + swz((kv0 + 9) * RBV + 16 * b + 4 * (r >> 1)));
-          const uint32_t sel = (r & 1) ? 0x7362u : 0x5140u;
-          const uint32_t x01 = prmt(w.x, w.y, sel), x89 = prmt(w.z, w.w, sel);
-          u4x4_to_f16x2x2(x01 & 0x0F0F0F0Fu, a_u0[0], a_u0[1]);
-          u4x4_to_f16x2x2(x89 & 0x0F0F0F0Fu, a_u0[2], a_u0[3]);
-          u4x4_to_f16x2x2((x01 >> 4) & 0x0F0F0F0Fu, a_u1[0], a_u1[1]);
-          u4x4_to_f16x2x2((x89 >> 4) & 0x0F0F0F0Fu, a_u1[2], a_u1[3]);
+          // chunk b is block b: low nibbles M-tile 2b, high nibbles (16 n) M-tile 2b+1
+          constexpr int BPG = NB < 4 ? NB : 4;
+#pragma unroll
+          for (int bb = 0; bb < BPG; ++bb) {
+            const int b = h * BPG + bb;
+            const uint32_t a_lo[4] = {q4_lo_even(w0[bb]), q4_lo_odd(w0[bb]), q4_lo_even(w1[bb]), q4_lo_odd(w1[bb])};
+            const uint32_t a_hi[4] = {q4_hi_even(w0[bb]), q4_hi_odd(w0[bb]), q4_hi_even(w1[bb]), q4_hi_odd(w1[bb])};
+            mma_16816(o_acc[2 * b], a_lo, bq[b]);
+            mma_16816(o_acc[2 * b + 1], a_hi, bq[b]);
+          }
         } else {
-          // fp16 values: zero the words of keys past the row so stale data never reaches the MMA
-          const bool ok0 = key0 + kv0 < ri.seq_len, ok1 = key0 + kv0 + 1 < ri.seq_len;
-          const bool ok8 = key0 + kv0 + 8 < ri.seq_len, ok9 = key0 + kv0 + 9 < ri.seq_len;
-          const int vo = 2 * (32 * b + 4 * r);
-          const uint2 e0 = ok0 ? lds64(vd + swz(kv0 * RBV + vo)) : make_uint2(0u, 0u);
-          const uint2 e1 = ok1 ? lds64(vd + swz((kv0 + 1) * RBV + vo)) : make_uint2(0u, 0u);
-          const uint2 e8 = ok8 ? lds64(vd + swz((kv0 + 8) * RBV + vo)) : make_uint2(0u, 0u);
-          const uint2 e9 = ok9 ? lds64(vd + swz((kv0 + 9) * RBV + vo)) : make_uint2(0u, 0u);
-          a_u0[0] = prmt(e0.x, e1.x, 0x5410u);
-          a_u0[1] = prmt(e0.x, e1.x, 0x7632u);
-          a_u0[2] = prmt(e8.x, e9.x, 0x5410u);
-          a_u0[3] = prmt(e8.x, e9.x, 0x7632u);
-          a_u1[0] = prmt(e0.y, e1.y, 0x5410u);
-          a_u1[1] = prmt(e0.y, e1.y, 0x7632u);
-          a_u1[2] = prmt(e8.y, e9.y, 0x5410u);
-          a_u1[3] = prmt(e8.y, e9.y, 0x7632u);
+          // fp16: chunks 4h..4h+3 (8 dims each) are rows 0-7 / 8-15 of M-tiles 2h, 2h+1
+          uint32_t mk0 = 0xFFFFFFFFu, mk1 = 0xFFFFFFFFu;
+          if (partial) {  // zero the keys past the row so stale data never reaches the MMA
+            mk0 = (key0 + kv0 < ri.seq_len ? 0x0000FFFFu : 0u) | (key0 + kv0 + 1 < ri.seq_len ? 0xFFFF0000u : 0u);
+            mk1 = (key0 + kv0 + 8 < ri.seq_len ? 0x0000FFFFu : 0u) | (key0 + kv0 + 9 < ri.seq_len ? 0xFFFF0000u : 0u);
+          }
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t a[4] = {w0[2 * j] & mk0, w0[2 * j + 1] & mk0, w1[2 * j] & mk1, w1[2 * j + 1] & mk1};
+            mma_16816(o_acc[2 * h + j], a, bq[0]);
+          }
         }
-        const uint32_t bop[2] = {bb[0], bb[1]};
-        mma_16816(o_acc[2 * b], a_u0, bop);
-        mma_16816(o_acc[2 * b + 1], a_u1, bop);
       }
     }
     __syncwarp();  // every lane is done with this stage before it is refilled
   }
   cp_async_wait<0>();
+
+  // ---------------- quantised V: take out the code offset and the 2^-24 ----------------
+  if (QV) {
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const float c0 = __shfl_sync(0xFFFFFFFFu, corr[0], 4 * b + c);
+      const float c1 = __shfl_sync(0xFFFFFFFFu, corr[1], 4 * b + c);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int tt = 2 * b + u;
+        const float f = (FV == MIXATTN_KV_Q4_0 && u == 1) ? 0.0625f : 1.f;
+        o_acc[tt][0] = fmaf(o_acc[tt][0], f, c0) * kTwo24;
+        o_acc[tt][1] = fmaf(o_acc[tt][1], f, c1) * kTwo24;
+        o_acc[tt][2] = fmaf(o_acc[tt][2], f, c0) * kTwo24;
+        o_acc[tt][3] = fmaf(o_acc[tt][3], f, c1) * kTwo24;
+      }
+    }
+  }
 
   // ---------------- warp partial -> shared memory ----------------
   l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 1);
