@@ -266,54 +266,6 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   //   (a2), the order of the subnormal pairs of one K word; for Q4_0 the j = 1
   //   k-step (high nibbles, 16 n) takes q / 16
   // fp16 K: k-step ks covers dims 16ks + 2c + {0, 1} (a0) and {8, 9} (a2)
-  // written once by warp 0 into the tile's Q block: word j (j < NB) of a lane holds the
-  // fragments of k-steps 2j, 2j+1 (a0, a2 each), word NB the four block starts, word
-  // NB + 1 the one-hot words of the value correction
-  const uint32_t q_s = smem_u32(smem) + S::q_off(NS);
-  if (warp == 0) {
-    uint32_t qa[KS][2];
-    float cb[4] = {0.f, 0.f, 0.f, 0.f};  // start of block b's score accumulator (head r)
-    const bool real = r < G;
-    const uint16_t* qrow =
-        static_cast<const uint16_t*>(p.q) + ((int64_t)ri.q_start * p.hq + (int64_t)g * G + (real ? r : 0)) * D;
-    if (!QK) {
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        qa[ks][0] = real ? ldg_u32(qrow + 16 * ks + 2 * c) : 0u;
-        qa[ks][1] = real ? ldg_u32(qrow + 16 * ks + 8 + 2 * c) : 0u;
-      }
-    } else {
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        float qs = 0.f;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          uint2 v = ldg_u64(qrow + 32 * b + 16 * j + 4 * c);
-          if (!real) v = make_uint2(0u, 0u);
-          qs += (h2f_lo(v.x) + h2f_hi(v.x)) + (h2f_lo(v.y) + h2f_hi(v.y));
-          uint32_t e = prmt(v.x, v.y, 0x5410u), o = prmt(v.x, v.y, 0x7632u);
-          if (FK == MIXATTN_KV_Q4_0 && j == 1) {
-            e = hmul2_u32(e, 0x2C002C00u);  // x 1/16
-            o = hmul2_u32(o, 0x2C002C00u);
-          }
-          qa[2 * b + j][0] = e;
-          qa[2 * b + j][1] = o;
-        }
-        qs += __shfl_xor_sync(0xFFFFFFFFu, qs, 1);
-        qs += __shfl_xor_sync(0xFFFFFFFFu, qs, 2);
-        cb[b] = qs * (FK == MIXATTN_KV_Q8_0 ? -128.f : -8.f) * kTwoM24;
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < NB; ++j)
-      sts128_s(q_s + 512 * j + 16 * lane, make_uint4(qa[2 * j][0], qa[2 * j][1], qa[2 * j + 1][0], qa[2 * j + 1][1]));
-    sts128_s(q_s + 512 * NB + 16 * lane,
-             make_uint4(__float_as_uint(cb[0]), __float_as_uint(cb[1]), __float_as_uint(cb[2]), __float_as_uint(cb[3])));
-    const uint32_t off = neg_offset_pair<FV>();
-    sts128_s(q_s + 512 * (NB + 1) + 16 * lane,
-             make_uint4(r == 0 ? off : 0u, r == 1 ? off : 0u, r == 2 ? off : 0u, r == 3 ? off : 0u));
-  }
-  decode_sync(half);
 
   float o_acc[KS][4];
 #pragma unroll
@@ -375,6 +327,56 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
 
 #pragma unroll
   for (int i = 0; i < NS - 1; ++i) issue(i);
+
+  // (after the first copies are under way) written once by warp 0 into the tile's Q
+  // block: word j (j < NB) of a lane holds the
+  // fragments of k-steps 2j, 2j+1 (a0, a2 each), word NB the four block starts, word
+  // NB + 1 the one-hot words of the value correction
+  const uint32_t q_s = smem_u32(smem) + S::q_off(NS);
+  if (warp == 0) {
+    uint32_t qa[KS][2];
+    float cb[4] = {0.f, 0.f, 0.f, 0.f};  // start of block b's score accumulator (head r)
+    const bool real = r < G;
+    const uint16_t* qrow =
+        static_cast<const uint16_t*>(p.q) + ((int64_t)ri.q_start * p.hq + (int64_t)g * G + (real ? r : 0)) * D;
+    if (!QK) {
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qa[ks][0] = real ? ldg_u32(qrow + 16 * ks + 2 * c) : 0u;
+        qa[ks][1] = real ? ldg_u32(qrow + 16 * ks + 8 + 2 * c) : 0u;
+      }
+    } else {
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        float qs = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          uint2 v = ldg_u64(qrow + 32 * b + 16 * j + 4 * c);
+          if (!real) v = make_uint2(0u, 0u);
+          qs += (h2f_lo(v.x) + h2f_hi(v.x)) + (h2f_lo(v.y) + h2f_hi(v.y));
+          uint32_t e = prmt(v.x, v.y, 0x5410u), o = prmt(v.x, v.y, 0x7632u);
+          if (FK == MIXATTN_KV_Q4_0 && j == 1) {
+            e = hmul2_u32(e, 0x2C002C00u);  // x 1/16
+            o = hmul2_u32(o, 0x2C002C00u);
+          }
+          qa[2 * b + j][0] = e;
+          qa[2 * b + j][1] = o;
+        }
+        qs += __shfl_xor_sync(0xFFFFFFFFu, qs, 1);
+        qs += __shfl_xor_sync(0xFFFFFFFFu, qs, 2);
+        cb[b] = qs * (FK == MIXATTN_KV_Q8_0 ? -128.f : -8.f) * kTwoM24;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+      sts128_s(q_s + 512 * j + 16 * lane, make_uint4(qa[2 * j][0], qa[2 * j][1], qa[2 * j + 1][0], qa[2 * j + 1][1]));
+    sts128_s(q_s + 512 * NB + 16 * lane,
+             make_uint4(__float_as_uint(cb[0]), __float_as_uint(cb[1]), __float_as_uint(cb[2]), __float_as_uint(cb[3])));
+    const uint32_t off = neg_offset_pair<FV>();
+    sts128_s(q_s + 512 * (NB + 1) + 16 * lane,
+             make_uint4(r == 0 ? off : 0u, r == 1 ? off : 0u, r == 2 ? off : 0u, r == 3 ? off : 0u));
+  }
+  decode_sync(half);
 
   // scale conversion: lanes 0-15 take the K scales of key lane, lanes 16-31 the V scales
   // of key lane - 16, into slot (key & 1) + 2 (key >> 3) of quad (key & 7) / 2
@@ -491,19 +493,20 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
         s[2] = key0 + kv0 + 8 < ri.seq_len ? s[2] : -CUDART_INF_F;
         s[3] = key0 + kv0 + 9 < ri.seq_len ? s[3] : -CUDART_INF_F;
       }
-      float pm = fmax3(s[0], s[1], fmaxf(s[2], s[3]));
-      pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 1));
-      pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 2));
-      pm *= sl2;  // scale > 0: the maximum of the scaled scores
-      // the running maximum only grows; alpha = 1 exactly when it stays (also -inf -> -inf)
-      const float m_new = fmaxf(m_run, pm);
-      const float alpha = m_new == m_run ? 1.f : ex2(m_run - m_new);
-      m_run = m_new;
-      const float mref = m_run == -CUDART_INF_F ? 0.f : m_run;
-      const float p0 = ex2(fmaf(s[0], sl2, -mref)), p1 = ex2(fmaf(s[1], sl2, -mref));
-      const float p8 = ex2(fmaf(s[2], sl2, -mref)), p9 = ex2(fmaf(s[3], sl2, -mref));
-      l_run = l_run * alpha + ((p0 + p1) + (p8 + p9));
-      if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+      // The reference m_run (per head, log2 units) follows the running maximum
+      // lazily: it moves, and O, corr and l are rescaled, only when a score passes it
+      // by more than kSlack.  Weights then stay <= 2^kSlack, so P' = p x scale stays
+      // finite in fp16 for every scale a format can hold (Q4_0 |d| <= 8188, Q8_0
+      // |d| <= 516), and the common M-tile needs one vote instead of a quad maximum.
+      constexpr float kSlack = FV == MIXATTN_KV_Q4_0 ? 2.f : (FV == MIXATTN_KV_Q8_0 ? 6.f : 8.f);
+      float pm = fmax3(s[0], s[1], fmaxf(s[2], s[3])) * sl2;  // this lane's maximum (scale > 0)
+      if (__any_sync(0xFFFFFFFFu, pm > m_run + kSlack)) {  // also the first valid key (m_run = -inf)
+        pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 1));
+        pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 2));
+        const bool grow = pm > m_run + kSlack;
+        const float alpha = grow ? ex2(m_run - pm) : 1.f;
+        m_run = grow ? pm : m_run;
+        l_run *= alpha;
         // O columns are heads 2c, 2c+1: their factors live in lanes 8c and 8c+4
         const float a_even = __shfl_sync(0xFFFFFFFFu, alpha, 8 * c);
         const float a_odd = __shfl_sync(0xFFFFFFFFu, alpha, 8 * c + 4);
@@ -517,6 +520,10 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
         corr[0] *= a_even;
         corr[1] *= a_odd;
       }
+      const float mref = m_run == -CUDART_INF_F ? 0.f : m_run;
+      const float p0 = ex2(fmaf(s[0], sl2, -mref)), p1 = ex2(fmaf(s[1], sl2, -mref));
+      const float p8 = ex2(fmaf(s[2], sl2, -mref)), p9 = ex2(fmaf(s[3], sl2, -mref));
+      l_run += (p0 + p1) + (p8 + p9);
 
       // ---------------- O^T += V^T P' for the 16 keys ----------------
       // P is already in the B-operand layout: this lane holds P[key kv0.., kv0+9][head r];
