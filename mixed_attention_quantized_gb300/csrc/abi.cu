@@ -194,13 +194,15 @@ int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* k
       const int ns = (int)((n_pages + pps - 1) / pps);
       rows[r].n_splits = ns;
       for (int g = 0; g < hkv; ++g) {
+        const int32_t first = (int32_t)decodes.size();  // partial slot of split 0
         for (int sp = 0; sp < ns; ++sp) {
           TileDesc t;
           t.row = r;
           t.kvh = g;
           t.begin = sp * pps;
           t.count = (int32_t)std::min<int64_t>(pps, n_pages - (int64_t)sp * pps);
-          t.kv0 = t.kv1 = t.part = 0;
+          t.kv0 = first;
+          t.kv1 = t.part = 0;
           t.nsplit = 1;
           decodes.push_back(t);
         }
@@ -210,8 +212,11 @@ int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* k
     if (total_q > INT32_MAX / std::max(hq, 1)) return MIXATTN_ERR_INVALID_ARG;
   }
   // heaviest chunk tiles first (they set the length of the launch), each cut
-  // into `split` consecutive pieces of its key range
+  // into `split` consecutive pieces of its key range; longest decode tiles first
+  // too, so the last wave holds the short ones (each keeps its partial slot)
   std::stable_sort(chunks.begin(), chunks.end(), [](const Chunk& a, const Chunk& b) { return a.cost > b.cost; });
+  std::stable_sort(decodes.begin(), decodes.end(),
+                   [](const TileDesc& a, const TileDesc& b) { return a.count > b.count; });
   int64_t n_pieces = 0;
   bool any_split = false;
   for (const Chunk& ch : chunks) {

@@ -233,8 +233,8 @@ __device__ __forceinline__ float h2f_hi(uint32_t x) { return __half2float(__usho
 //           added to the block's rows at the end.
 // The 2^24 is folded into the softmax scale (scores) and the epilogue (values).
 template <int FK, int FV, int D, int NS>
-__device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc& t, int dec_idx, uint8_t* smem,
-                                            unsigned int* err, int half) {
+__device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc& t, uint8_t* smem, unsigned int* err,
+                                            int half) {
   using S = DecodeSmem<FK, FV, D>;
   constexpr int NB = D / kBlock;   // scale blocks per row
   constexpr int KS = D / 16;       // k-steps of QK / M-tiles of PV
@@ -645,7 +645,7 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   const int n_out = G * D;
   const int n_warps_used = min(kWarps, (t.count + ppw - 1) / ppw);
   const bool single = ri.n_splits == 1;
-  float* part = p.partials + (int64_t)dec_idx * G * (D + 2);
+  float* part = p.partials + (int64_t)(t.kv0 + split) * G * (D + 2);  // t.kv0: slot of split 0
   for (int idx = tid; idx < n_out; idx += kThreads) {
     const int h = idx / D, d = idx - h * D;
     float mmax = -CUDART_INF_F;
@@ -682,7 +682,7 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   decode_sync(half);
   if (!s_last) return;
   __threadfence();
-  const int first = dec_idx - split;
+  const int first = t.kv0;
   const int ns = ri.n_splits;
   for (int idx = tid; idx < n_out; idx += kThreads) {
     const int h = idx / D, d = idx - h * D;
@@ -1350,8 +1350,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) mixed_attention_kernel(AttnP
     if (half && !FS::kTwoDecode) return;
     const int d = FS::kDecodePerCta * (tile - p.n_chunk_ctas) + half;
     if (d >= p.n_decode_tiles) return;
-    decode_tile<FK, FV, D, FS::kDecodeStages>(p, p.tiles[p.n_chunk_tiles + d], d, smem + half * FS::kHalfBytes, err,
-                                              half);
+    decode_tile<FK, FV, D, FS::kDecodeStages>(p, p.tiles[p.n_chunk_tiles + d], smem + half * FS::kHalfBytes, err, half);
   }
 }
 
@@ -1359,7 +1358,7 @@ template <int FK, int FV, int D, int MINB, int NS>
 __global__ void __launch_bounds__(kThreads, MINB) decode_attention_kernel(AttnParams p, unsigned int* err) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tile = blockIdx.x + p.n_chunk_tiles;
-  decode_tile<FK, FV, D, NS>(p, p.tiles[tile], blockIdx.x, smem, err, 0);
+  decode_tile<FK, FV, D, NS>(p, p.tiles[tile], smem, err, 0);
 }
 
 // Chunk tiles whose mean KV-tile count is below this are walked by persistent

@@ -43,7 +43,9 @@ struct RowInfo {
 //           against 128-key KV tiles kv0 .. kv1-1; a tile whose key range is cut
 //           into nsplit pieces (part = 0 .. nsplit-1, consecutive in the tile
 //           list) leaves partial results that the last piece to finish merges
-//   decode: pages begin .. begin+count-1 of `row`, kv head kvh (kv0..nsplit unused)
+//   decode: pages begin .. begin+count-1 of `row`, kv head kvh; kv0 = partial slot of
+//           the (row, kv head)'s first split (its splits take slots kv0 .. kv0+n_splits-1,
+//           wherever the tiles sit in the list); kv1..nsplit unused
 struct TileDesc {
   int32_t row;
   int32_t kvh;

@@ -146,9 +146,12 @@ int tile_into_upload(const mixattn_kv_cache& c, int hq, int n_rows, const int32_
       const int pps = decode_pages_per_split((int)n_pages);
       const int ns = (int)((n_pages + pps - 1) / pps);
       rows[r].n_splits = ns;
-      for (int g = 0; g < hkv; ++g)
+      for (int g = 0; g < hkv; ++g) {
+        const int32_t first = (int32_t)(id - n_chunk);  // partial slot of split 0
         for (int sp = 0; sp < ns; ++sp)
-          tiles[id++] = TileDesc{r, g, sp * pps, (int32_t)std::min<int64_t>(pps, n_pages - (int64_t)sp * pps), 0, 0, 0, 1};
+          tiles[id++] =
+              TileDesc{r, g, sp * pps, (int32_t)std::min<int64_t>(pps, n_pages - (int64_t)sp * pps), first, 0, 0, 1};
+      }
     }
     q0 += nq;
   }
@@ -161,6 +164,13 @@ int tile_into_upload(const mixattn_kv_cache& c, int hq, int n_rows, const int32_
   std::sort(tiles, tiles + n_chunk, [&](const TileDesc& a, const TileDesc& b) {
     const int64_t ca = cost(a), cb = cost(b);
     if (ca != cb) return ca > cb;
+    if (a.row != b.row) return a.row < b.row;
+    if (a.kvh != b.kvh) return a.kvh < b.kvh;
+    return a.begin < b.begin;
+  });
+  // longest decode tiles first; ties in row order (each keeps its partial slot)
+  std::sort(tiles + n_chunk, tiles + n_tiles, [](const TileDesc& a, const TileDesc& b) {
+    if (a.count != b.count) return a.count > b.count;
     if (a.row != b.row) return a.row < b.row;
     if (a.kvh != b.kvh) return a.kvh < b.kvh;
     return a.begin < b.begin;
