@@ -59,13 +59,15 @@ struct TileDesc {
 
 // Pages each warp of a decode CTA walks, a function of the row's own length
 // only (so a row's result does not depend on the other rows of the batch):
-// about 8 splits per (row, kv head) up to 2048 pages, then splits of 256 pages.
+// about 4 splits per (row, kv head) up to 1024 pages, then splits of 256 pages.
 // Fewer, longer splits measured faster wherever a batch fills the GPU: each
-// split pays a fixed set-up and its partial is merged serially by the last CTA
-// of the (row, kv head) (e.g. a 262144-token row: 186 -> 160 us with 32 instead
-// of 128 splits).
+// split pays a fixed set-up (page ids, first copies, Q, the warp merge) and its
+// partial is merged serially by the last CTA of the (row, kv head).  Against ~8
+// splits: 64 rows x 8192 tokens Q4_0 0.40 -> 0.47 of HBM, Q8_0 0.66 -> 0.75; the
+// serving mix 209 -> 200 us; one 8192-token row alone 0.090 -> 0.076 (it fills
+// only 32 CTAs).
 MIXATTN_HD int decode_pages_per_warp(int n_pages) {
-  int p = (n_pages + 63) / 64;
+  int p = (n_pages + 31) / 32;
   return p < 1 ? 1 : (p > 32 ? 32 : p);
 }
 

@@ -56,10 +56,10 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls_in_a_row():
 def test_noalloc_rejects_a_batch_beyond_its_scratch():
     import torch
     import mixed_attention_quantized_gb300 as mq
-    # 128 decode rows at ctx 32768 share one 1024-page cache: 128 x 8 kv heads x 8 split
+    # 256 decode rows at ctx 32768 share one 1024-page cache: 256 x 8 kv heads x 4 split
     # tiles of ~2 KB partials each is ~17 MB of workspace, over the 16 MiB the library
     # holds.  Every input is valid, so the request is refused on its size alone.
-    n_rows, ctx = 128, 32768
+    n_rows, ctx = 256, 32768
     cache = mq.KVCache.allocate(ctx // 32, 8, 128, wl.FMT_Q8_0, wl.FMT_Q8_0)
     q = torch.zeros((n_rows, 32, 128), dtype=torch.float16, device="cuda")
     pt = torch.arange(ctx // 32, dtype=torch.int32, device="cuda").repeat(n_rows, 1).contiguous()
