@@ -515,7 +515,7 @@ def main():
         "roofline": roof,
         "e2e": {"value": whole_job_tokens_per_s(alg["tokens"], world, res["e2e_ms"]), "unit": "tokens/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
-        "gpu_launches": 2 * K,
+        "gpu_launches": 3 * K,  # per step: append, tile-list upload, attention
         "clocks": res["clocks"],
         "plan": res["plan"],
         "device_error": res["device_error"],

@@ -198,8 +198,10 @@ int mixattn_plan_info(const mixattn_plan* plan, int32_t* total_q, int32_t* n_chu
  *   o           device fp16 [total_q][num_q_heads][head_dim], 16-byte aligned
  *   workspace   device, >= workspace_bytes of the plan, 256-byte aligned; its
  *               contents need not be initialised and are overwritten
- * The call is asynchronous on `stream`: it enqueues one host-to-device copy of
- * the tile list (from the plan's pinned buffer) and one kernel.  Runs of the
+ * The call is asynchronous on `stream`: it enqueues two kernels, one that reads
+ * the tile list from the plan's mapped pinned buffer into the workspace (no
+ * copy-engine transfer, so it never waits behind the caller's own host-to-device
+ * copies on other streams) and the attention kernel.  Runs of the
  * same plan on different streams must not overlap (they share the buffer only
  * for reading; the workspace is the caller's).
  */

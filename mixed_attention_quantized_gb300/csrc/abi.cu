@@ -267,7 +267,8 @@ struct mixattn_plan {
   mixattn_kv_cache cache;
   int32_t hq = 0, group = 0, log2_group = 0, n_rows = 0, max_pages = 0;
   Tiling tiling;
-  uint8_t* host_buf = nullptr;  // pinned copy of tiling.image
+  uint8_t* host_buf = nullptr;  // pinned, mapped copy of tiling.image
+  const uint8_t* host_dev = nullptr;  // the same buffer as the device sees it
   size_t host_cap = 0;
   cudaEvent_t copied = nullptr;
   bool copy_recorded = false;
@@ -288,12 +289,21 @@ int plan_fill(mixattn_plan* p, int32_t n_rows, const int32_t* kinds, const int32
   if (t.image.size() > p->host_cap) {
     if (p->host_buf) cudaFreeHost(p->host_buf);
     p->host_buf = nullptr;
+    p->host_dev = nullptr;
     p->host_cap = 0;
     size_t cap = std::max<size_t>(t.image.size(), 4096);
-    if (cudaHostAlloc(reinterpret_cast<void**>(&p->host_buf), cap, cudaHostAllocDefault) != cudaSuccess) {
+    if (cudaHostAlloc(reinterpret_cast<void**>(&p->host_buf), cap, cudaHostAllocMapped | cudaHostAllocPortable) !=
+        cudaSuccess) {
       p->host_buf = nullptr;
       return MIXATTN_ERR_CUDA;
     }
+    void* dv = nullptr;
+    if (cudaHostGetDevicePointer(&dv, p->host_buf, 0) != cudaSuccess || !dv) {
+      cudaFreeHost(p->host_buf);
+      p->host_buf = nullptr;
+      return MIXATTN_ERR_CUDA;
+    }
+    p->host_dev = static_cast<const uint8_t*>(dv);
     p->host_cap = cap;
   }
   memcpy(p->host_buf, t.image.data(), t.image.size());
@@ -392,6 +402,13 @@ int mixattn_plan_info(const mixattn_plan* plan, int32_t* total_q, int32_t* n_chu
   return MIXATTN_OK;
 }
 
+// Copies n16 16-byte words of a plan's tile list from its mapped pinned buffer
+// into the workspace.
+static __global__ void upload_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n16) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
 int mixattn_run(const mixattn_plan* plan_c, const void* q, const int32_t* page_table, void* o, void* workspace,
                 size_t workspace_bytes, mixattn_stream stream) {
   mixattn_plan* plan = const_cast<mixattn_plan*>(plan_c);
@@ -404,9 +421,16 @@ int mixattn_run(const mixattn_plan* plan_c, const void* q, const int32_t* page_t
   if (!err) return MIXATTN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (cudaMemcpyAsync(ws + L.rows, plan->host_buf, L.upload_end - L.rows, cudaMemcpyHostToDevice, s) !=
-      cudaSuccess)
-    return MIXATTN_ERR_CUDA;
+  // the tile list comes in through a small kernel reading the mapped pinned buffer
+  // rather than a copy-engine transfer, which would queue behind any large
+  // host-to-device copy the caller has in flight on another stream
+  {
+    const size_t n16 = (L.upload_end - L.rows) / 16;
+    const int blocks = (int)std::min<size_t>((n16 + 255) / 256, 128);
+    upload_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(plan->host_dev),
+                                         reinterpret_cast<uint4*>(ws + L.rows), n16);
+    if (cudaGetLastError() != cudaSuccess) return MIXATTN_ERR_CUDA;
+  }
   if (cudaEventRecord(plan->copied, s) != cudaSuccess) return MIXATTN_ERR_CUDA;
   plan->copy_recorded = true;
 
