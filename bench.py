@@ -493,7 +493,7 @@ def main():
     else:
         roof = {"bound": "tensor", "achieved": tflops, "peak": peaks["tflops"], "unit": "TFLOP/s",
                 "frac": tflops / peaks["tflops"]}
-    roof["traffic"] = measured_traffic(w.name)
+    roof["traffic"] = measured_traffic(args.workload)  # keyed by the workload as named on the command line
     roof["peak_source"] = peaks["source"]
     roof["kernel"] = "mixattn fused attention (one launch per step)"
     roof["roofline_time_frac"] = max(t_bytes, t_flops) / attn_s
