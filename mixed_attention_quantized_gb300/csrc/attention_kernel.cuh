@@ -257,8 +257,11 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   const int ppw = decode_pages_per_warp(n_pages_row);
   const int pps = kWarps * ppw;
   const int split = t.begin / pps;
-  const int wp0 = t.begin + warp * ppw;
-  const int wp1 = min(t.begin + t.count, wp0 + ppw);
+  // the tile's pages spread evenly over its 8 warps (runs differing by at most one
+  // page, each at most ppw), so a row's shorter last split also keeps every warp busy
+  const int pg_base = t.count / kWarps, pg_rem = t.count - pg_base * kWarps;
+  const int wp0 = t.begin + warp * pg_base + min(warp, pg_rem);
+  const int wp1 = wp0 + pg_base + (warp < pg_rem ? 1 : 0);
   const int n_mt = wp1 > wp0 ? 2 * (wp1 - wp0) : 0;  // the warp's M-tiles (16 keys each)
 
   // ---- Q as the A operand of S = Q K^T: head r in M row r (rows 8..15 zero) ----
@@ -643,7 +646,7 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
 
   // ---------------- merge the 8 warps ----------------
   const int n_out = G * D;
-  const int n_warps_used = min(kWarps, (t.count + ppw - 1) / ppw);
+  const int n_warps_used = min(kWarps, t.count);
   const bool single = ri.n_splits == 1;
   float* part = p.partials + (int64_t)(t.kv0 + split) * G * (D + 2);  // t.kv0: slot of split 0
   for (int idx = tid; idx < n_out; idx += kThreads) {
