@@ -178,3 +178,21 @@ def test_cut_chunk_tiles_match_oracle_and_stay_row_independent():
     q = torch.from_numpy(wl.queries(w)[:256].copy()).cuda()
     alone = run_attention(one, cache, pt[:1], q=q)
     assert np.array_equal(alone, full[:256])
+
+
+@pytest.mark.parametrize("kf,vf", [(wl.FMT_Q8_0, wl.FMT_Q8_0), (wl.FMT_Q4_0, wl.FMT_Q4_0), (wl.FMT_Q8_0, wl.FMT_Q4_0)])
+def test_values_near_the_fp16_limit_stay_finite(kf, vf):
+    """V values up to 6e4 (block scales near the largest a format can hold) and
+    queries x4 (sharp scores, frequent new maxima): weights relative to a lagging
+    softmax reference times those scales must stay inside fp16, and the error
+    scales with the values (the 2e-3 budget per unit of V, plus the fp16 rounding
+    of the output itself)."""
+    gain = 12000.0
+    rows = [(D, 3000, 2999), (D, 700, 699), (D, 33, 32), (C, 300, 200)]
+    w = wl.custom("near_limit", 32, 8, 128, kf, vf, 21, rows, v_gain=gain, q_gain=4.0)
+    cache, pt = build_cache(w)
+    out = run_attention(w, cache, pt).astype(np.float64)
+    ref = oracle_attention(w)
+    assert np.isfinite(out).all()
+    assert (np.abs(out - ref) <= TOL * gain + np.abs(ref) * 2.0 ** -11).all(), np.abs(out - ref).max()
+

@@ -53,6 +53,8 @@ class Workload:
     alpha: float = 8.0
     page_size: int = PAGE
     spare_pages: int = 0
+    v_gain: float = 1.0  # V values multiplied by this (then kept inside +-60000)
+    q_gain: float = 1.0  # queries multiplied by this (sharper scores)
 
     @property
     def n_rows(self) -> int:
@@ -99,20 +101,22 @@ def outlier_channels(w: Workload) -> np.ndarray:
                      for _ in range(w.num_kv_heads)])
 
 
-def _normal_f16(key: Tuple[int, ...], shape, scale_cols=None) -> np.ndarray:
+def _normal_f16(key: Tuple[int, ...], shape, scale_cols=None, gain: float = 1.0) -> np.ndarray:
     x = _rng(*key).standard_normal(size=shape, dtype=np.float32)
     if scale_cols is not None:
         x = x * scale_cols
+    if gain != 1.0:
+        x = np.clip(x * np.float32(gain), -60000.0, 60000.0)
     return x.astype(np.float16)
 
 
 def _blocked(w: Workload, r: int, tensor: int, start: int, stop: int, width_shape,
-             scale_cols=None) -> np.ndarray:
+             scale_cols=None, gain: float = 1.0) -> np.ndarray:
     out = np.empty((stop - start,) + tuple(width_shape), dtype=np.float16)
     b0, b1 = start // TOKEN_BLOCK, (stop - 1) // TOKEN_BLOCK if stop > start else -1
     for b in range(b0, b1 + 1):
         lo, hi = b * TOKEN_BLOCK, (b + 1) * TOKEN_BLOCK
-        blk = _normal_f16((w.seed, r, tensor, b), (TOKEN_BLOCK,) + tuple(width_shape), scale_cols)
+        blk = _normal_f16((w.seed, r, tensor, b), (TOKEN_BLOCK,) + tuple(width_shape), scale_cols, gain)
         s, e = max(lo, start), min(hi, stop)
         out[s - start:e - start] = blk[s - lo:e - lo]
     return out
@@ -128,13 +132,13 @@ def row_kv(w: Workload, r: int, start: int = 0, stop: Optional[int] = None):
         for g, chans in enumerate(outlier_channels(w)):
             cols[g, chans] = np.float32(w.alpha)
     k = _blocked(w, r, _T_K, start, stop, shape, cols)
-    v = _blocked(w, r, _T_V, start, stop, shape)
+    v = _blocked(w, r, _T_V, start, stop, shape, gain=w.v_gain)
     return k, v
 
 
 def row_q(w: Workload, r: int) -> np.ndarray:
     """fp16 queries ``[q_len, Hq, D]`` of row r (positions q_offset .. seq_len-1)."""
-    return _blocked(w, r, _T_Q, w.q_offsets[r], w.seq_lens[r], (w.num_q_heads, w.head_dim))
+    return _blocked(w, r, _T_Q, w.q_offsets[r], w.seq_lens[r], (w.num_q_heads, w.head_dim), gain=w.q_gain)
 
 
 def queries(w: Workload) -> np.ndarray:
@@ -220,8 +224,8 @@ def decode_sweep(batch: int, ctx: int, fmt: int) -> Workload:
 
 def custom(name: str, hq: int, hkv: int, d: int, k_fmt: int, v_fmt: int, seed: int,
            rows: List[Tuple[int, int, int]], n_outlier: int = 0, alpha: float = 8.0,
-           spare_pages: int = 0) -> Workload:
+           spare_pages: int = 0, v_gain: float = 1.0, q_gain: float = 1.0) -> Workload:
     """Free-form workload; rows are (kind, seq_len, q_offset)."""
     return Workload(name, hq, hkv, d, k_fmt, v_fmt, seed, [r[0] for r in rows],
                     [r[1] for r in rows], [r[2] for r in rows], n_outlier, alpha,
-                    spare_pages=spare_pages)
+                    spare_pages=spare_pages, v_gain=v_gain, q_gain=q_gain)
