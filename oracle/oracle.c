@@ -14,11 +14,11 @@
  *    occupancy table: bytes per KV position 2048 / 1088 / 832 / 576.
  *  - same page, §1 "統一 mixed-batch 介面": chunk rows and decode rows share
  *    one ForwardBatch and one attention kernel.
- *  - The block formulas are the GGUF Q8_0 / Q4_0 conventions the same page
- *    invokes ("支援主流的gguf"): Q8_0 d = amax/127, q = round(x/d);
+ *  - The block formulas are the GGUF Q8_0 / Q4_0 conventions of the model
+ *    files the same page says the engine reads: Q8_0 d = amax/127, q = round(x/d);
  *    Q4_0 d = (signed max)/-8, q = min(15, trunc(x/d + 8.5)), x^ = (q-8)*d.
  *
- * Readings where the pages leave a step open (each also listed in the design doc):
+ * Readings where the pages leave a step open:
  *  - blocks run along head_dim, per (token, kv head);
  *  - q is computed as x * id with id = 1/d in fp32 (d in fp32); only the stored
  *    scale is rounded to fp16 (round-to-nearest-even);
