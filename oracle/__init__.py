@@ -76,6 +76,8 @@ def _load():
                 ctypes.c_int, i32p, i32p, u16p, u8p, i64p, u8p, i64p, ctypes.c_int,
                 i32p, f64p, ctypes.c_int]
             lib.orc_attention.restype = ctypes.c_int
+            lib.orc_attention_window.argtypes = lib.orc_attention.argtypes + [ctypes.c_int]
+            lib.orc_attention_window.restype = ctypes.c_int
             lib.orc_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -141,8 +143,11 @@ def dequantize(fmt: int, blocks) -> np.ndarray:
 
 
 def attention(fmt_k: int, fmt_v: int, q, k_blocks, v_blocks, seq_lens, q_offsets,
-              sel=None, threads: int = 0) -> np.ndarray:
+              sel=None, threads: int = 0, window: int = 0) -> np.ndarray:
     """fp64 causal attention over the dequantised cache.
+
+    window:    > 0 for sliding-window attention: the query at position p sees
+               keys p - window + 1 .. p only; 0 (default) sees keys 0 .. p.
 
     q:         fp16 ``[total_q, Hq, D]``, rows packed in order.
     k_blocks:  list (one per row) of uint8 ``[seq_len, Hkv, D/32, bb]`` canonical blocks.
@@ -176,12 +181,12 @@ def attention(fmt_k: int, fmt_v: int, q, k_blocks, v_blocks, seq_lens, q_offsets
         sel = np.arange(total_q, dtype=np.int32)
     sel = np.ascontiguousarray(sel, dtype=np.int32)
     out = np.empty((len(sel), hq, d), dtype=np.float64)
-    rc = _load().orc_attention(
+    rc = _load().orc_attention_window(
         int(fmt_k), int(fmt_v), d, hq, hkv, n_rows, _ptr(seq_lens, ctypes.c_int32),
         _ptr(q_offsets, ctypes.c_int32), _ptr(q.view(np.uint16), ctypes.c_uint16),
         _ptr(k_all, ctypes.c_uint8), _ptr(k_off, ctypes.c_int64), _ptr(v_all, ctypes.c_uint8),
         _ptr(v_off, ctypes.c_int64), len(sel), _ptr(sel, ctypes.c_int32),
-        _ptr(out, ctypes.c_double), int(threads))
+        _ptr(out, ctypes.c_double), int(threads), int(window))
     if rc != 0:
         raise RuntimeError(f"orc_attention failed ({rc})")
     return out

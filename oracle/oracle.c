@@ -238,11 +238,15 @@ static int find_row(int n_rows, const int32_t* q_start, const int32_t* n_q, int3
   return -1;
 }
 
-int orc_attention(int fmt_k, int fmt_v, int D, int Hq, int Hkv, int n_rows,
-                  const int32_t* seq_len, const int32_t* q_offset,
-                  const uint16_t* q_f16, const uint8_t* k_blocks, const int64_t* k_off,
-                  const uint8_t* v_blocks, const int64_t* v_off, int n_sel,
-                  const int32_t* sel, double* out, int n_threads) {
+/* window > 0: sliding-window attention -- the query at position p sees only */
+/* the `window` most recent keys, p - window + 1 .. p (the page's per-model   */
+/* table, Gemma 4 row: its SWA layers read the same Q8 cache).  window <= 0:  */
+/* every key 0 .. p.                                                          */
+int orc_attention_window(int fmt_k, int fmt_v, int D, int Hq, int Hkv, int n_rows,
+                         const int32_t* seq_len, const int32_t* q_offset,
+                         const uint16_t* q_f16, const uint8_t* k_blocks, const int64_t* k_off,
+                         const uint8_t* v_blocks, const int64_t* v_off, int n_sel,
+                         const int32_t* sel, double* out, int n_threads, int window) {
   if (D % ORC_QK != 0 || Hkv <= 0 || Hq % Hkv != 0) return -1;
   int bbk = orc_block_bytes(fmt_k), bbv = orc_block_bytes(fmt_v);
   if (bbk < 0 || bbv < 0) return -1;
@@ -276,11 +280,12 @@ int orc_attention(int fmt_k, int fmt_v, int D, int Hq, int Hkv, int n_rows,
     int g = h / G;
     int p = q_offset[r] + (t - q_start[r]); /* position of this query */
     int nkeys = p + 1;                     /* causal: keys 0..p */
+    int first = (window > 0 && p + 1 > window) ? p + 1 - window : 0; /* sliding window */
     double q[512], kh[512], vh[512];
     for (int d = 0; d < D; ++d) q[d] = (double)orc_f16_to_f32(q_f16[((int64_t)t * Hq + h) * D + d]);
     double* s = (double*)malloc(sizeof(double) * (size_t)nkeys);
     double smax = -INFINITY;
-    for (int j = 0; j < nkeys; ++j) {
+    for (int j = first; j < nkeys; ++j) {
       const uint8_t* kb = k_blocks + k_off[r] + (((int64_t)j * Hkv + g) * nb) * bbk;
       for (int b = 0; b < nb; ++b) dequant_block(fmt_k, kb + b * bbk, kh + b * ORC_QK);
       double dot = 0.0;
@@ -291,7 +296,7 @@ int orc_attention(int fmt_k, int fmt_v, int D, int Hq, int Hkv, int n_rows,
     double denom = 0.0;
     double o[512];
     for (int d = 0; d < D; ++d) o[d] = 0.0;
-    for (int j = 0; j < nkeys; ++j) {
+    for (int j = first; j < nkeys; ++j) {
       double w = exp(s[j] - smax);
       denom += w;
       const uint8_t* vb = v_blocks + v_off[r] + (((int64_t)j * Hkv + g) * nb) * bbv;
@@ -305,6 +310,15 @@ int orc_attention(int fmt_k, int fmt_v, int D, int Hq, int Hkv, int n_rows,
   free(q_start);
   free(n_q);
   return status;
+}
+
+int orc_attention(int fmt_k, int fmt_v, int D, int Hq, int Hkv, int n_rows,
+                  const int32_t* seq_len, const int32_t* q_offset,
+                  const uint16_t* q_f16, const uint8_t* k_blocks, const int64_t* k_off,
+                  const uint8_t* v_blocks, const int64_t* v_off, int n_sel,
+                  const int32_t* sel, double* out, int n_threads) {
+  return orc_attention_window(fmt_k, fmt_v, D, Hq, Hkv, n_rows, seq_len, q_offset, q_f16, k_blocks, k_off,
+                              v_blocks, v_off, n_sel, sel, out, n_threads, 0);
 }
 
 int orc_max_threads(void) {

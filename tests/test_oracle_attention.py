@@ -21,8 +21,9 @@ def _cache_blocks(w, r, fmt_k, fmt_v):
     return oracle.quantize(fmt_k, k), oracle.quantize(fmt_v, v)
 
 
-def _sdpa_reference(w, kb, vb):
-    """torch fp64 SDPA over the oracle-dequantised K/V, row by row."""
+def _sdpa_reference(w, kb, vb, window=0):
+    """torch fp64 SDPA over the oracle-dequantised K/V, row by row (window > 0:
+    a band mask, key j visible to position p iff p - window < j <= p)."""
     q = wl.queries(w)
     out = []
     g = w.num_q_heads // w.num_kv_heads
@@ -36,6 +37,8 @@ def _sdpa_reference(w, kb, vb):
         vt = torch.from_numpy(vd).permute(1, 0, 2)[None]
         pos = torch.arange(off, s)[:, None]
         mask = torch.arange(s)[None, :] <= pos  # key j visible to the query at position p iff j <= p
+        if window > 0:
+            mask = mask & (torch.arange(s)[None, :] > pos - window)
         o = torch.nn.functional.scaled_dot_product_attention(qr, kt, vt, attn_mask=mask,
                                                              enable_gqa=(g > 1))
         out.append(o[0].permute(1, 0, 2).numpy())
@@ -143,3 +146,66 @@ def test_workload_shapes_follow_the_configs():
     k, v = wl.row_kv(s, 3)
     k2, v2 = wl.row_kv(s, 3, 4000, 4200)
     assert np.array_equal(k[4000:4200], k2) and np.array_equal(v[4000:4200], v2)
+
+
+# ---------------------------------------------------------------------------
+# Sliding-window attention (the page's per-model table, Gemma 4 row: its SWA
+# layers read the same Q8 cache).  Reading: a window of W keys ends at the
+# query's own position, keys p - W + 1 .. p.
+# ---------------------------------------------------------------------------
+
+def _window_case(fmt_k, fmt_v, seed=13):
+    rows = [(wl.ROW_CHUNK, 150, 40), (wl.ROW_DECODE, 300, 299), (wl.ROW_DECODE, 5, 4), (wl.ROW_CHUNK, 70, 0)]
+    return wl.custom("win", 8, 2, 64, fmt_k, fmt_v, seed=seed, rows=rows, n_outlier=2)
+
+
+@pytest.mark.parametrize("window", [1, 2, 31, 32, 33, 100, 1000])
+@pytest.mark.parametrize("fmt_k,fmt_v", [(wl.FMT_F16, wl.FMT_F16), (wl.FMT_Q8_0, wl.FMT_Q4_0)])
+def test_window_matches_torch_sdpa_band_mask(fmt_k, fmt_v, window):
+    w = _window_case(fmt_k, fmt_v)
+    kb, vb = zip(*[_cache_blocks(w, r, fmt_k, fmt_v) for r in range(w.n_rows)])
+    got = oracle.attention(fmt_k, fmt_v, wl.queries(w), kb, vb, w.seq_lens, w.q_offsets, window=window)
+    np.testing.assert_allclose(got, _sdpa_reference(w, kb, vb, window=window), rtol=1e-10, atol=1e-12)
+
+
+def test_window_of_one_returns_the_own_value():
+    fmt = wl.FMT_Q8_0
+    w = _window_case(fmt, fmt)
+    kb, vb = zip(*[_cache_blocks(w, r, fmt, fmt) for r in range(w.n_rows)])
+    got = oracle.attention(fmt, fmt, wl.queries(w), kb, vb, w.seq_lens, w.q_offsets, window=1)
+    for r in range(w.n_rows):
+        vd = oracle.dequantize(fmt, vb[r]).reshape(w.seq_lens[r], 2, 64)
+        for i in range(w.q_lens[r]):
+            p = w.q_offsets[r] + i
+            for h in range(8):
+                assert np.array_equal(got[w.q_starts[r] + i, h], vd[p, h // 4])
+
+
+def test_window_at_least_the_sequence_is_full_attention():
+    fmt = wl.FMT_Q4_0
+    w = _window_case(fmt, fmt)
+    kb, vb = zip(*[_cache_blocks(w, r, fmt, fmt) for r in range(w.n_rows)])
+    q = wl.queries(w)
+    full = oracle.attention(fmt, fmt, q, kb, vb, w.seq_lens, w.q_offsets)
+    assert np.array_equal(oracle.attention(fmt, fmt, q, kb, vb, w.seq_lens, w.q_offsets, window=300), full)
+    assert not np.array_equal(oracle.attention(fmt, fmt, q, kb, vb, w.seq_lens, w.q_offsets, window=299), full)
+
+
+def test_window_equals_full_attention_over_the_last_keys():
+    """A query at position p with window W sees exactly what a decode row sees
+    whose cache holds only keys p - W + 1 .. p (the full-attention oracle,
+    pinned above, on a truncated cache)."""
+    fmt = wl.FMT_Q8_0
+    w = _window_case(fmt, fmt)
+    kb, vb = zip(*[_cache_blocks(w, r, fmt, fmt) for r in range(w.n_rows)])
+    q = wl.queries(w)
+    W = 37
+    got = oracle.attention(fmt, fmt, q, kb, vb, w.seq_lens, w.q_offsets, window=W)
+    for r in (0, 1):
+        for i in sorted({0, min(5, w.q_lens[r] - 1), w.q_lens[r] - 1}):
+            t = w.q_starts[r] + i
+            p = w.q_offsets[r] + i
+            lo = max(0, p - W + 1)
+            n = p + 1 - lo
+            ref = oracle.attention(fmt, fmt, q[t:t + 1], [kb[r][lo:p + 1]], [vb[r][lo:p + 1]], [n], [n - 1])
+            assert np.array_equal(got[t], ref[0])
