@@ -51,11 +51,21 @@ def make_workload(name: str) -> wl.Workload:
         return wl.long_session(wl.FMT_Q4_0)
     if name == "fairness":
         return wl.fairness()
-    if name.startswith("sweep_"):  # sweep_<batch>_<ctx>_<f16|q8_0|q4_0>
+    if name.startswith("sweep_"):  # sweep_<batch>_<ctx>_<f16|q8_0|q4_0|k8v4|k4v8>
         _, b, c, f = name.split("_", 3)
+        mixed = {"k8v4": (wl.FMT_Q8_0, wl.FMT_Q4_0), "k4v8": (wl.FMT_Q4_0, wl.FMT_Q8_0)}
+        if f in mixed:
+            return wl.decode_sweep(int(b), int(c), *mixed[f])
         fmt = {v: k for k, v in wl.FMT_NAMES.items()}[f]
         return wl.decode_sweep(int(b), int(c), fmt)
     raise SystemExit(f"unknown workload {name}")
+
+
+# The other KV formats of the metric, measured after the headline workload by a
+# default run (one sub-object each): the tensor-bound fairness chunk (Q4_0), the
+# long session in both formats, and one fp16 and one K8V4 decode-sweep point.
+FORMAT_WORKLOADS = [("fairness", 10), ("long_session_q8", 50), ("long_session_q4", 50),
+                    ("sweep_4_65536_f16", 50), ("sweep_16_8192_k8v4", 50)]
 
 
 # --------------------------------------------------------------------------
@@ -215,6 +225,97 @@ def step_inputs(w: wl.Workload, pt: np.ndarray):
     return np.concatenate(ks), np.concatenate(vs), np.concatenate(ss).astype(np.int32)
 
 
+def prepare(w: wl.Workload, dev):
+    """The cache with every row's history appended, the step's inputs on the
+    device and a plan with its workspace."""
+    import torch
+    import mixed_attention_quantized_gb300 as mq
+    cache = mq.KVCache.allocate(w.num_pages, w.num_kv_heads, w.head_dim, w.k_fmt, w.v_fmt, device=dev)
+    pt = wl.page_table(w)
+    for r in range(w.n_rows):
+        for s0 in range(0, w.seq_lens[r], 65536):
+            s1 = min(w.seq_lens[r], s0 + 65536)
+            k, v = wl.row_kv(w, r, s0, s1)
+            mq.kv_append_quant(cache, torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev),
+                               torch.from_numpy(wl.slots(w, pt, r, s0, s1)).to(dev))
+    k_new, v_new, slots = step_inputs(w, pt)
+    d = {"cache": cache, "pt": pt, "k_new": k_new, "v_new": v_new, "slots": slots, "q_host": wl.queries(w)}
+    d["kd"] = torch.from_numpy(k_new).to(dev)
+    d["vd"] = torch.from_numpy(v_new).to(dev)
+    d["sd"] = torch.from_numpy(slots).to(dev)
+    d["qd"] = torch.from_numpy(d["q_host"]).to(dev)
+    d["ptd"] = torch.from_numpy(pt).to(dev)
+    d["od"] = torch.empty_like(d["qd"])
+    d["plan"] = mq.Plan(cache, w.num_q_heads, w.row_kinds, w.seq_lens, w.q_offsets, pt.shape[1])
+    d["ws"] = mq.alloc_workspace(d["plan"].workspace_bytes, dev)
+    return d
+
+
+def time_steps(d, steps: int, warmup: int, dev, stream):
+    """Per-step CUDA-event times (ms) of the append and the attention (upload +
+    fused launch) on the launching stream, after `warmup` untimed steps."""
+    import torch
+    import mixed_attention_quantized_gb300 as mq
+    cache, plan = d["cache"], d["plan"]
+    for _ in range(warmup):
+        mq.kv_append_quant(cache, d["kd"], d["vd"], d["sd"], stream)
+        plan.run(d["qd"], d["ptd"], d["od"], d["ws"], stream)
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        mq.kv_append_quant(cache, d["kd"], d["vd"], d["sd"], stream)
+        ev[i][1].record(stream)
+        plan.run(d["qd"], d["ptd"], d["od"], d["ws"], stream)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    return ([ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)],
+            [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)])
+
+
+def roofline_of(w: wl.Workload, alg: dict, attn_s: float, peaks: dict, traffic_key: str) -> dict:
+    t_bytes = alg["attn_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_flops = alg["chunk_flops"] / (peaks["tflops"] * 1e12)
+    if t_bytes >= t_flops:
+        gbs = alg["attn_bytes"] / attn_s / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"]}
+    else:
+        tf = alg["chunk_flops"] / attn_s / 1e12
+        roof = {"bound": "tensor", "achieved": tf, "peak": peaks["tflops"], "unit": "TFLOP/s",
+                "frac": tf / peaks["tflops"]}
+    roof["traffic"] = measured_traffic(traffic_key)
+    roof["peak_source"] = peaks["source"]
+    roof["roofline_time_frac"] = max(t_bytes, t_flops) / attn_s
+    return roof
+
+
+def measure_format(name: str, steps: int, warmup: int, dev, stream, peaks: dict, stride: int,
+                   cpu: bool) -> dict:
+    """One sub-object of the default run: a workload in another KV format."""
+    import torch
+    w = make_workload(name)
+    alg = algorithmic(w)
+    d = prepare(w, dev)
+    app_ms, attn_ms = time_steps(d, steps, warmup, dev, stream)
+    d["plan"].close()
+    del d
+    torch.cuda.empty_cache()
+    attn = sum(attn_ms) / len(attn_ms)
+    app = sum(app_ms) / len(app_ms)
+    out = {"workload": w.name, "kv_format": f"K={wl.FMT_NAMES[w.k_fmt]},V={wl.FMT_NAMES[w.v_fmt]}",
+           "steps": steps, "tokens_per_step": alg["tokens"],
+           "value": alg["tokens"] / ((attn + app) / 1e3), "unit": "tokens/s",
+           "attention_us": attn * 1e3, "append_us": app * 1e3,
+           "kv_gbs": alg["kv_bytes"] / (attn / 1e3) / 1e9,
+           "kv_frac_of_hbm": alg["kv_bytes"] / (attn / 1e3) / 1e9 / peaks["hbm_gbs"],
+           "chunk_tflops": alg["chunk_flops"] / (attn / 1e3) / 1e12,
+           "roofline": roofline_of(w, alg, attn / 1e3, peaks, name)}
+    if cpu:
+        out["cpu_baseline"] = cpu_baseline(w, stride if w.name != "fairness" else 64)
+    return out
+
+
 def run_gpu(args, rank: int, world: int, local_rank: int) -> dict:
     import torch
     import mixed_attention_quantized_gb300 as mq
@@ -223,25 +324,12 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict:
     dev = torch.device("cuda", local_rank)
     w = make_workload(args.workload)
     alg = algorithmic(w)
-    cache = mq.KVCache.allocate(w.num_pages, w.num_kv_heads, w.head_dim, w.k_fmt, w.v_fmt, device=dev)
-    pt = wl.page_table(w)
-    # the history of every row (the new tokens are appended again by every step)
-    for r in range(w.n_rows):
-        for s0 in range(0, w.seq_lens[r], 65536):
-            s1 = min(w.seq_lens[r], s0 + 65536)
-            k, v = wl.row_kv(w, r, s0, s1)
-            mq.kv_append_quant(cache, torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev),
-                               torch.from_numpy(wl.slots(w, pt, r, s0, s1)).to(dev))
-    k_new, v_new, slots = step_inputs(w, pt)
-    q_host = wl.queries(w)
-    kd = torch.from_numpy(k_new).to(dev)
-    vd = torch.from_numpy(v_new).to(dev)
-    sd = torch.from_numpy(slots).to(dev)
-    qd = torch.from_numpy(q_host).to(dev)
-    ptd = torch.from_numpy(pt).to(dev)
-    od = torch.empty_like(qd)
-    plan = mq.Plan(cache, w.num_q_heads, w.row_kinds, w.seq_lens, w.q_offsets, pt.shape[1])
-    ws = mq.alloc_workspace(plan.workspace_bytes, dev)
+    # the history of every row is in the cache; each step appends its new tokens again
+    d = prepare(w, dev)
+    cache, pt, plan, ws = d["cache"], d["pt"], d["plan"], d["ws"]
+    k_new, v_new, slots, q_host = d["k_new"], d["v_new"], d["slots"], d["q_host"]
+    kd, vd, sd, qd, ptd, od = d["kd"], d["vd"], d["sd"], d["qd"], d["ptd"], d["od"]
+    del d
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -355,9 +443,20 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict:
 
     plan_info = plan.info()
     plan.close()
+    del cache, bufs, dev_blobs, kd, vd, sd, qd, ptd, od, ws
+    torch.cuda.empty_cache()
+    # the other KV formats (default run on one GPU): each its own sub-object
+    formats = []
+    if args.formats and world == 1:
+        for name, steps in FORMAT_WORKLOADS:
+            if name == args.workload:
+                continue
+            formats.append(measure_format(name, min(steps, args.steps), 3, dev, stream, load_peaks(),
+                                          args.oracle_stride, not args.no_cpu_baseline))
+        dev_err |= mq.device_error(clear=True)
     return {"w": w, "alg": alg, "total_ms": total_ms, "attn_ms": attn_mean, "append_ms": app_mean,
             "attn_ms_list": attn_ms, "clocks": clocks, "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
-            "plan": plan_info, "device_error": dev_err}
+            "plan": plan_info, "device_error": dev_err, "formats": formats}
 
 
 # --------------------------------------------------------------------------
@@ -432,7 +531,11 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--oracle-stride", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-formats", dest="formats", action="store_false",
+                    help="skip the other KV formats' sub-measurements of the default run")
     args = ap.parse_args()
+    if args.workload != "serving_mix":
+        args.formats = False
     if args.warmup < 3:
         args.warmup = 3
 
@@ -489,20 +592,9 @@ def main():
     value = whole_job_tokens_per_s(alg["tokens"], world, ms_step)
     attn_s = res["attn_ms"] / 1e3
     kv_gbs = alg["kv_bytes"] / attn_s / 1e9
-    attn_gbs = alg["attn_bytes"] / attn_s / 1e9
     tflops = alg["chunk_flops"] / attn_s / 1e12
-    t_bytes = alg["attn_bytes"] / (peaks["hbm_gbs"] * 1e9)
-    t_flops = alg["chunk_flops"] / (peaks["tflops"] * 1e12)
-    if t_bytes >= t_flops:
-        roof = {"bound": "hbm", "achieved": attn_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": attn_gbs / peaks["hbm_gbs"]}
-    else:
-        roof = {"bound": "tensor", "achieved": tflops, "peak": peaks["tflops"], "unit": "TFLOP/s",
-                "frac": tflops / peaks["tflops"]}
-    roof["traffic"] = measured_traffic(args.workload)  # keyed by the workload as named on the command line
-    roof["peak_source"] = peaks["source"]
+    roof = roofline_of(w, alg, attn_s, peaks, args.workload)  # traffic keyed by the workload's CLI name
     roof["kernel"] = "mixattn fused attention (one launch per step)"
-    roof["roofline_time_frac"] = max(t_bytes, t_flops) / attn_s
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
@@ -526,6 +618,8 @@ def main():
         "plan": res["plan"],
         "device_error": res["device_error"],
     }
+    if res["formats"]:
+        line["formats"] = res["formats"]
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.oracle_stride)
     emit(line, rank)

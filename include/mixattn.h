@@ -27,9 +27,24 @@
  *     validation happens before any launch; on an error nothing is launched.
  *   - Kernels check page ids and slots on the device.  A bad one sets a bit in
  *     a device error word and the offending page or token is skipped (no trap);
- *     read and clear it with mixattn_device_error().
+ *     read and clear it with mixattn_device_error().  A decode split or chunk
+ *     piece whose every page was skipped has no keys: its outputs are NaN.
+ *   - Device checks surface at the next call: once a kernel has set an error
+ *     bit on a device (a bad page id or slot, or a bounded wait that gave up),
+ *     every later call of mixattn_kv_append_quant, mixattn_kv_export_blocks,
+ *     mixattn_run and mixattn_mixed_attention on that device returns
+ *     MIXATTN_ERR_DEVICE_CHECK and launches nothing, until
+ *     mixattn_device_error(1) clears the word.  The host learns of it through
+ *     a pinned, host-mapped flag that the kernels set beside the word, so the
+ *     check costs no synchronisation; it sees kernels that have finished, and
+ *     the first mixattn_plan_create on a device arms it (before that, and on
+ *     the no-allocation entry point, only mixattn_device_error reports).
  *   - No call allocates device memory.  mixattn_plan_create allocates one
- *     pinned host buffer, owned by the plan.
+ *     pinned host buffer, owned by the plan, and the first one on a device a
+ *     64-byte pinned flag that lives until the process exits.
+ *   - Outputs are rounded to the nearest fp16, saturating at +-65504: a Q8_0
+ *     block whose largest element is 65504 dequantises it to 127 * 516 = 65532,
+ *     and a mean dominated by such values stays finite.
  */
 #ifndef MIXATTN_H
 #define MIXATTN_H
@@ -173,6 +188,19 @@ int mixattn_plan_create(mixattn_plan** plan_out, const mixattn_kv_cache* cache, 
                         int32_t n_rows, const int32_t* row_kinds, const int32_t* seq_lens,
                         const int32_t* q_offsets, int32_t max_pages, size_t* workspace_bytes);
 
+/*
+ * The same with a sliding window (reference page, §2 per-model table: the
+ * Gemma 4 row's SWA layers read the same Q8 cache): every query at position p
+ * sees keys max(0, p - window + 1) .. p only; window 0 is full causal attention
+ * (mixattn_plan_create).  The tiling skips the pages and KV tiles before each
+ * row's window, so a decode row reads ~window keys whatever its length.  A
+ * model with both layer kinds keeps one plan per kind over the same batch.
+ * window < 0 -> MIXATTN_ERR_INVALID_ARG.  mixattn_plan_update keeps the window.
+ */
+int mixattn_plan_create_window(mixattn_plan** plan_out, const mixattn_kv_cache* cache, int32_t num_q_heads,
+                               int32_t window, int32_t n_rows, const int32_t* row_kinds, const int32_t* seq_lens,
+                               const int32_t* q_offsets, int32_t max_pages, size_t* workspace_bytes);
+
 /* Re-tile an existing plan for a new batch (same cache and heads), reusing its
  * pinned buffer when it is large enough.  Waits for the plan's previous
  * mixattn_run to have copied the old tile list before overwriting it. */
@@ -212,9 +240,12 @@ void mixattn_plan_destroy(mixattn_plan* plan);
 
 /*
  * One call: mixed_attention(q, page_table, seq_lens, q_offsets, row_kinds) -> o.
- * Plans, runs and frees the plan.  The host waits for the tile-list copy
- * before returning (the plan's buffer is freed).  workspace as for mixattn_run;
- * query its size with mixattn_workspace_bytes.
+ * A convenience path that synchronises: it plans (allocating the plan's pinned
+ * buffer), runs, and frees the plan, and freeing pinned memory waits for the
+ * device, so the call returns only after the stream's work up to the attention
+ * launch has finished.  A serving loop should keep a plan and call
+ * mixattn_plan_update + mixattn_run instead, which never wait.  workspace as
+ * for mixattn_run; query its size with mixattn_workspace_bytes.
  */
 int mixattn_mixed_attention(const mixattn_kv_cache* cache, int32_t num_q_heads, const void* q,
                             const int32_t* page_table, int32_t max_pages, int32_t n_rows,

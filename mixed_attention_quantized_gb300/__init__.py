@@ -29,17 +29,31 @@ LIB_PATH = os.path.join(_HERE, "libmixattn.so")
 
 EXPORTED = [
     "mixattn_kv_cache_bytes", "mixattn_kv_append_quant", "mixattn_kv_export_blocks",
-    "mixattn_plan_create", "mixattn_plan_update", "mixattn_plan_info", "mixattn_run",
+    "mixattn_plan_create", "mixattn_plan_create_window", "mixattn_plan_update", "mixattn_plan_info", "mixattn_run",
     "mixattn_plan_destroy", "mixattn_mixed_attention", "mixattn_workspace_bytes",
     "mixattn_device_error", "mixattn_status_string", "mixattn_version",
     "mixattn_mixed_attention_noalloc",
+    "mixattn_sched_default_config", "mixattn_sched_create", "mixattn_sched_destroy", "mixattn_sched_submit",
+    "mixattn_sched_next_batch", "mixattn_sched_complete", "mixattn_sched_request_info", "mixattn_sched_counts",
 ]
+
+ERR_CLIENT_QUOTA = -6
+STEP_IDLE, STEP_DECODE, STEP_MERGED, STEP_PREFILL = 0, 1, 2, 3
+REQ_WAITING, REQ_PREFILL, REQ_DECODE, REQ_DONE = 0, 1, 2, 3
 
 
 class MixattnError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
         super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class SchedConfig(ctypes.Structure):
+    _fields_ = [
+        ("max_sessions", ctypes.c_int32), ("prefill_chunk", ctypes.c_int32),
+        ("max_pending_per_client", ctypes.c_int32), ("near_done_tokens", ctypes.c_int32),
+        ("max_decode_rows", ctypes.c_int32),
+    ]
 
 
 class KVCacheDesc(ctypes.Structure):
@@ -78,6 +92,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.mixattn_plan_create.argtypes = [ctypes.POINTER(vp), cachep, i32, i32, i32p, i32p, i32p, i32,
                                         ctypes.POINTER(sz)]
     lib.mixattn_plan_create.restype = ctypes.c_int
+    lib.mixattn_plan_create_window.argtypes = [ctypes.POINTER(vp), cachep, i32, i32, i32, i32p, i32p, i32p, i32,
+                                               ctypes.POINTER(sz)]
+    lib.mixattn_plan_create_window.restype = ctypes.c_int
     lib.mixattn_plan_update.argtypes = [vp, i32, i32p, i32p, i32p, i32, ctypes.POINTER(sz)]
     lib.mixattn_plan_update.restype = ctypes.c_int
     lib.mixattn_plan_info.argtypes = [vp, i32p, i32p, i32p]
@@ -98,6 +115,24 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.mixattn_status_string.restype = ctypes.c_char_p
     lib.mixattn_version.argtypes = []
     lib.mixattn_version.restype = i32
+    cfgp = ctypes.POINTER(SchedConfig)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    lib.mixattn_sched_default_config.argtypes = [cfgp]
+    lib.mixattn_sched_default_config.restype = None
+    lib.mixattn_sched_create.argtypes = [ctypes.POINTER(vp), cfgp]
+    lib.mixattn_sched_create.restype = ctypes.c_int
+    lib.mixattn_sched_destroy.argtypes = [vp]
+    lib.mixattn_sched_destroy.restype = None
+    lib.mixattn_sched_submit.argtypes = [vp, i64, i32, i32, i32]
+    lib.mixattn_sched_submit.restype = ctypes.c_int
+    lib.mixattn_sched_next_batch.argtypes = [vp, i32, i32p, i32p, i32p, i64p, i32p]
+    lib.mixattn_sched_next_batch.restype = i32
+    lib.mixattn_sched_complete.argtypes = [vp, i64p, i32]
+    lib.mixattn_sched_complete.restype = ctypes.c_int
+    lib.mixattn_sched_request_info.argtypes = [vp, i64, i32p, i32p, i32p, i64p, i64p]
+    lib.mixattn_sched_request_info.restype = ctypes.c_int
+    lib.mixattn_sched_counts.argtypes = [vp, i32p, i32p, i32p, i64p]
+    lib.mixattn_sched_counts.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -211,21 +246,23 @@ def kv_export_blocks(cache: KVCache, which: int, slots, stream=None):
 
 
 class Plan:
-    """Host tiling of one ForwardBatch; reusable across layers and re-tileable."""
+    """Host tiling of one ForwardBatch; reusable across layers and re-tileable.
+    ``window`` > 0 makes every run sliding-window attention (keys p-window+1..p)."""
 
     def __init__(self, cache: KVCache, num_q_heads: int, row_kinds, seq_lens, q_offsets,
-                 max_pages: int):
+                 max_pages: int, window: int = 0):
         self._lib = load()
         self.cache = cache
         self.num_q_heads = int(num_q_heads)
+        self.window = int(window)
         self._handle = ctypes.c_void_p(0)
         ws = ctypes.c_size_t(0)
         self._desc = cache.desc()
         n = len(seq_lens)
-        st = self._lib.mixattn_plan_create(ctypes.byref(self._handle), ctypes.byref(self._desc),
-                                           self.num_q_heads, n, _i32_array(row_kinds),
-                                           _i32_array(seq_lens), _i32_array(q_offsets),
-                                           int(max_pages), ctypes.byref(ws))
+        st = self._lib.mixattn_plan_create_window(ctypes.byref(self._handle), ctypes.byref(self._desc),
+                                                  self.num_q_heads, self.window, n, _i32_array(row_kinds),
+                                                  _i32_array(seq_lens), _i32_array(q_offsets),
+                                                  int(max_pages), ctypes.byref(ws))
         _check(st, "mixattn_plan_create")
         self.workspace_bytes = int(ws.value)
 
@@ -324,3 +361,90 @@ def device_error(clear: bool = False) -> int:
 
 def version() -> int:
     return int(load().mixattn_version())
+
+
+@dataclass
+class Batch:
+    """One step built by the fair batch builder: the attention ABI's row arrays."""
+    kind: int
+    row_kinds: list
+    seq_lens: list
+    q_offsets: list
+    request_ids: list
+
+
+class FairBatchBuilder:
+    """The host fair batch builder (``include/mixattn_sched.h``): requests in,
+    ForwardBatch row arrays out (decode first, one bounded prefill slice per
+    step, SRTF, starvation preemption behind the near-done gate,
+    MarkAllDecodersDue, PopDecoder rotation, per-client admission)."""
+
+    def __init__(self, max_sessions: int = 16, prefill_chunk: int = 512, max_pending_per_client: int = 0,
+                 near_done_tokens: int = 64, max_decode_rows: int = 0):
+        self._lib = load()
+        self.config = SchedConfig(max_sessions, prefill_chunk, max_pending_per_client, near_done_tokens,
+                                  max_decode_rows)
+        self._h = ctypes.c_void_p(0)
+        _check(self._lib.mixattn_sched_create(ctypes.byref(self._h), ctypes.byref(self.config)),
+               "mixattn_sched_create")
+        cap = max_sessions + 1
+        self._cap = cap
+        self._kinds = (ctypes.c_int32 * cap)()
+        self._seq = (ctypes.c_int32 * cap)()
+        self._off = (ctypes.c_int32 * cap)()
+        self._ids = (ctypes.c_int64 * cap)()
+
+    @staticmethod
+    def default_config() -> SchedConfig:
+        c = SchedConfig()
+        load().mixattn_sched_default_config(ctypes.byref(c))
+        return c
+
+    def submit(self, request_id: int, client_id: int, prompt_len: int, max_new_tokens: int) -> int:
+        """Queue a request; returns OK or ERR_CLIENT_QUOTA (other statuses raise)."""
+        st = self._lib.mixattn_sched_submit(self._h, int(request_id), int(client_id), int(prompt_len),
+                                            int(max_new_tokens))
+        if st not in (OK, ERR_CLIENT_QUOTA):
+            _check(st, "mixattn_sched_submit")
+        return st
+
+    def next_batch(self) -> Batch:
+        kind = ctypes.c_int32(0)
+        n = self._lib.mixattn_sched_next_batch(self._h, self._cap, self._kinds, self._seq, self._off, self._ids,
+                                               ctypes.byref(kind))
+        if n < 0:
+            _check(n, "mixattn_sched_next_batch")
+        return Batch(kind.value, list(self._kinds[:n]), list(self._seq[:n]), list(self._off[:n]),
+                     list(self._ids[:n]))
+
+    def complete(self, stop_ids=()) -> None:
+        ids = list(stop_ids)
+        arr = (ctypes.c_int64 * max(1, len(ids)))(*ids)
+        _check(self._lib.mixattn_sched_complete(self._h, arr, len(ids)), "mixattn_sched_complete")
+
+    def info(self, request_id: int) -> dict:
+        st, ca, ge = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        ft, dn = ctypes.c_int64(), ctypes.c_int64()
+        _check(self._lib.mixattn_sched_request_info(self._h, int(request_id), ctypes.byref(st), ctypes.byref(ca),
+                                                    ctypes.byref(ge), ctypes.byref(ft), ctypes.byref(dn)),
+               "mixattn_sched_request_info")
+        return {"state": st.value, "cached": ca.value, "generated": ge.value, "first_token_step": ft.value,
+                "done_step": dn.value}
+
+    def counts(self) -> dict:
+        w, p, d = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        n = ctypes.c_int64()
+        _check(self._lib.mixattn_sched_counts(self._h, ctypes.byref(w), ctypes.byref(p), ctypes.byref(d),
+                                              ctypes.byref(n)), "mixattn_sched_counts")
+        return {"waiting": w.value, "prefills": p.value, "decoders": d.value, "steps": n.value}
+
+    def close(self) -> None:
+        if self._h and self._h.value:
+            self._lib.mixattn_sched_destroy(self._h)
+            self._h = ctypes.c_void_p(0)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

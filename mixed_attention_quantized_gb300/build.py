@@ -32,14 +32,22 @@ def _nvcc() -> str:
 
 
 def sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    """CUDA translation units (nvcc) and host-only C++ ones (g++)."""
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cc")))
 
 
 def _inputs():
     files = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))
-    files.append(os.path.join(REPO, "include", "mixattn.h"))
+    files += glob.glob(os.path.join(REPO, "include", "*.h"))
     files.append(os.path.abspath(__file__))
     return files
+
+
+def _cxx() -> str:
+    for cand in (os.environ.get("CXX"), shutil.which("g++"), shutil.which("c++")):
+        if cand and shutil.which(cand):
+            return cand
+    raise RuntimeError("no C++ compiler found (g++) for the host-only sources")
 
 
 def up_to_date() -> bool:
@@ -58,8 +66,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *CFLAGS, *extra, "-c", src, "-o", obj]
+        base, ext = os.path.splitext(os.path.basename(src))
+        obj = os.path.join(OUT_DIR, base + ext.replace(".", "_") + ".o")
+        if ext == ".cc":  # host-only C++: the plain host compiler, same language level
+            cmd = [_cxx(), "-O2", "-std=c++17", "-fPIC", "-DNDEBUG", "-I", os.path.join(REPO, "include"),
+                   "-c", src, "-o", obj]
+        else:
+            cmd = [nvcc, *ARCH, *CFLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")

@@ -15,27 +15,85 @@
 #include <queue>
 #include <vector>
 
+#include "../../include/mixattn_sched.h"
 #include "internal.h"
 
 namespace mixattn {
 
-__device__ unsigned int g_device_error = 0u;
+// Per device: word 0 = OR of MIXATTN_DEVERR_* bits set by kernels; words 2-3 =
+// device address of the host-mapped flag that kernels also set (0 until armed).
+__device__ __align__(16) unsigned int g_device_error[4] = {0u, 0u, 0u, 0u};
 
 namespace {
 
-// Address of this device's error word (kernels receive it as an argument).
+std::mutex g_err_mu;
+unsigned int* g_err_word[kMaxDevices] = {};          // device address of g_device_error
+volatile unsigned int* g_err_flag[kMaxDevices] = {};  // host view of the armed flag
+
+// Address of this device's error block (kernels receive it as an argument).
 unsigned int* error_word() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  static std::mutex mu;
-  static unsigned int* ptrs[64] = {};
-  std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_err_mu);
+  if (!g_err_word[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<unsigned int*>(p);
+    g_err_word[dev] = static_cast<unsigned int*>(p);
   }
-  return ptrs[dev];
+  return g_err_word[dev];
+}
+
+// Arms the host-mapped flag of the current device (once): a pinned, mapped
+// word whose device address is stored in the error block, so kernels that set
+// an error bit also set the flag and the next call sees it without touching
+// the device.  The copy runs on a private non-blocking stream in relaxed
+// capture mode, so it neither waits for nor disturbs the caller's streams.
+// Failure leaves the device unarmed (calls then cannot report earlier checks,
+// mixattn_device_error still can).
+void arm_device_check() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
+  if (!error_word()) return;
+  std::lock_guard<std::mutex> lock(g_err_mu);
+  if (g_err_flag[dev]) return;
+  cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+  if (cudaThreadExchangeStreamCaptureMode(&mode) != cudaSuccess) return;
+  unsigned int* host = nullptr;
+  void* dptr = nullptr;
+  cudaStream_t st = nullptr;
+  bool ok = cudaHostAlloc(reinterpret_cast<void**>(&host), 64, cudaHostAllocMapped | cudaHostAllocPortable) ==
+            cudaSuccess;
+  if (ok) {
+    host[0] = 0u;
+    reinterpret_cast<void**>(host)[1] = nullptr;
+    ok = cudaHostGetDevicePointer(&dptr, host, 0) == cudaSuccess && dptr;
+  }
+  if (ok) {
+    reinterpret_cast<void**>(host)[1] = dptr;  // the value copied into words 2-3
+    ok = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess;
+  }
+  if (ok) {
+    ok = cudaMemcpyToSymbolAsync(g_device_error, reinterpret_cast<void**>(host) + 1, sizeof(void*),
+                                 2 * sizeof(unsigned int), cudaMemcpyHostToDevice, st) == cudaSuccess &&
+         cudaStreamSynchronize(st) == cudaSuccess;
+  }
+  if (st) cudaStreamDestroy(st);
+  if (ok) {
+    g_err_flag[dev] = host;
+  } else {
+    if (host) cudaFreeHost(host);
+    cudaGetLastError();  // nothing of this is the caller's error
+  }
+  cudaThreadExchangeStreamCaptureMode(&mode);
+}
+
+// MIXATTN_ERR_DEVICE_CHECK when a kernel on the current device has set an error
+// bit since the last clear (seen through the armed flag), else MIXATTN_OK.
+int pending_device_check() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MIXATTN_OK;
+  volatile unsigned int* f = g_err_flag[dev];
+  return (f && *f) ? MIXATTN_ERR_DEVICE_CHECK : MIXATTN_OK;
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -79,6 +137,7 @@ cudaError_t dispatch_attention(int k_fmt, int v_fmt, int head_dim, const AttnPar
 struct Tiling {
   std::vector<uint8_t> image;  // [rows | tiles | counters], from WorkspaceLayout::rows
   int32_t total_q = 0, n_chunk = 0, n_decode = 0;
+  int32_t slot_rows = 0;       // rows of a decode partial slot
   int32_t chunk_kv_tiles = 0;  // KV tiles over all chunk tiles (their mean decides persistence)
   WorkspaceLayout L{};
 };
@@ -132,18 +191,21 @@ int chunk_split_factor(const std::vector<int64_t>& costs, int n_sm) {
 }
 
 int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* kinds, const int32_t* seq,
-                 const int32_t* off, int max_pages, int n_sm, Tiling* out) {
-  if (n_rows <= 0 || !kinds || !seq || !off || max_pages <= 0) return MIXATTN_ERR_INVALID_ARG;
+                 const int32_t* off, int max_pages, int n_sm, int window, Tiling* out) {
+  if (n_rows <= 0 || !kinds || !seq || !off || max_pages <= 0 || window < 0) return MIXATTN_ERR_INVALID_ARG;
   if (hq <= 0 || hq % c.num_kv_heads != 0) return MIXATTN_ERR_INVALID_ARG;
   const int G = hq / c.num_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return MIXATTN_ERR_UNSUPPORTED;
   const int hkv = c.num_kv_heads;
   const int T = kChunkM / G;  // query tokens per chunk tile
+  const int QPG = kMaxGroup / G;  // queries per decode-style tile of a verify row
+  bool any_verify = false;
 
   std::vector<RowInfo> rows(n_rows);
   struct Chunk {
     TileDesc t;
-    int64_t cost;
+    int64_t kv_first;  // first KV tile the tile's queries can see
+    int64_t cost;      // KV tiles from there to the last query's key
     int split;
   };
   std::vector<Chunk> chunks;
@@ -166,7 +228,11 @@ int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* k
     rows[r].q_offset = (int32_t)o;
     rows[r].n_splits = 0;
     const int64_t nq = s - o;
-    if (kinds[r] == MIXATTN_ROW_CHUNK) {
+    // a short chunk row (speculative verify: q_len * G <= kVerifyMaxRows) runs like decode
+    // rows, on split-K tiles of up to 8 (query, head) rows
+    const bool verify = kinds[r] == MIXATTN_ROW_CHUNK && nq * G <= kVerifyMaxRows;
+    any_verify = any_verify || verify;
+    if (kinds[r] == MIXATTN_ROW_CHUNK && !verify) {
       const size_t first_chunk = chunks.size();
       for (int g = 0; g < hkv; ++g) {
         for (int64_t b = 0; b < nq; b += T) {
@@ -178,7 +244,9 @@ int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* k
           ch.t.kv0 = ch.t.kv1 = ch.t.part = 0;
           ch.t.nsplit = 1;
           const int64_t key_end = std::min<int64_t>(s, o + b + ch.t.count);
-          ch.cost = (key_end + kChunkN - 1) / kChunkN;
+          // a sliding window skips the KV tiles before the first query's first key
+          ch.kv_first = window_first_key((int)(o + b), window) / kChunkN;
+          ch.cost = (key_end + kChunkN - 1) / kChunkN - ch.kv_first;
           ch.split = 1;
           chunks.push_back(ch);
         }
@@ -190,21 +258,28 @@ int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* k
       const int split = chunk_split_factor(costs, n_sm);
       for (size_t i = first_chunk; i < chunks.size(); ++i) chunks[i].split = split;
     } else {
-      const int pps = decode_pages_per_split((int)n_pages);
-      const int ns = (int)((n_pages + pps - 1) / pps);
+      // pages from the one holding the first query's window start (page 0 without a
+      // window) to the last; the split size depends on the row alone
+      const int64_t first_page = window_first_key((int)o, window) / kPage;
+      const int64_t n_win = n_pages - first_page;
+      const int pps = decode_pages_per_split((int)n_win);
+      const int ns = (int)((n_win + pps - 1) / pps);
       rows[r].n_splits = ns;
       for (int g = 0; g < hkv; ++g) {
-        const int32_t first = (int32_t)decodes.size();  // partial slot of split 0
-        for (int sp = 0; sp < ns; ++sp) {
-          TileDesc t;
-          t.row = r;
-          t.kvh = g;
-          t.begin = sp * pps;
-          t.count = (int32_t)std::min<int64_t>(pps, n_pages - (int64_t)sp * pps);
-          t.kv0 = first;
-          t.kv1 = t.part = 0;
-          t.nsplit = 1;
-          decodes.push_back(t);
+        for (int64_t qg = 0; qg < nq; qg += QPG) {
+          const int32_t first = (int32_t)decodes.size();  // partial slot of split 0
+          for (int sp = 0; sp < ns; ++sp) {
+            TileDesc t;
+            t.row = r;
+            t.kvh = g;
+            t.begin = (int32_t)(first_page + (int64_t)sp * pps);
+            t.count = (int32_t)std::min<int64_t>(pps, n_win - (int64_t)sp * pps);
+            t.kv0 = first;
+            t.kv1 = (int32_t)qg;                                  // the group's first query
+            t.part = sp;
+            t.nsplit = (int32_t)std::min<int64_t>(QPG, nq - qg);  // the group's queries
+            decodes.push_back(t);
+          }
         }
       }
     }
@@ -230,19 +305,20 @@ int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* k
   T2.total_q = (int32_t)total_q;
   T2.n_chunk = (int32_t)n_pieces;
   T2.n_decode = (int32_t)decodes.size();
-  T2.L = workspace_layout(n_rows, (int)n_tiles, T2.n_decode, hkv, G, c.head_dim, any_split);
+  T2.slot_rows = any_verify ? kMaxGroup : G;
+  T2.L = workspace_layout(n_rows, (int)n_tiles, T2.n_decode, T2.slot_rows, c.head_dim, any_split);
   T2.image.assign(T2.L.upload_end - T2.L.rows, 0);
   memcpy(T2.image.data(), rows.data(), sizeof(RowInfo) * rows.size());
   TileDesc* td = reinterpret_cast<TileDesc*>(T2.image.data() + (T2.L.tiles - T2.L.rows));
   int64_t at = 0, kv_tiles = 0;
   for (size_t i = 0; i < chunks.size(); ++i) {
-    const int64_t n_kv = chunks[i].cost;
+    const int64_t n_kv = chunks[i].cost, kv_first = chunks[i].kv_first;
     kv_tiles += n_kv;
     const int split = chunks[i].split;
     for (int q = 0; q < split; ++q) {
       TileDesc t = chunks[i].t;
-      t.kv0 = (int32_t)((n_kv * q) / split);
-      t.kv1 = (int32_t)((n_kv * (q + 1)) / split);
+      t.kv0 = (int32_t)(kv_first + (n_kv * q) / split);
+      t.kv1 = (int32_t)(kv_first + (n_kv * (q + 1)) / split);
       t.part = q;
       t.nsplit = split;
       td[at++] = t;
@@ -266,6 +342,7 @@ using namespace mixattn;
 struct mixattn_plan {
   mixattn_kv_cache cache;
   int32_t hq = 0, group = 0, log2_group = 0, n_rows = 0, max_pages = 0;
+  int32_t window = 0;  // sliding window of every run of the plan (0: full causal attention)
   Tiling tiling;
   uint8_t* host_buf = nullptr;  // pinned, mapped copy of tiling.image
   const uint8_t* host_dev = nullptr;  // the same buffer as the device sees it
@@ -279,7 +356,7 @@ namespace {
 int plan_fill(mixattn_plan* p, int32_t n_rows, const int32_t* kinds, const int32_t* seq, const int32_t* off,
               int32_t max_pages, size_t* ws_bytes) {
   Tiling t;
-  int st = build_tiling(p->cache, p->hq, n_rows, kinds, seq, off, max_pages, device_sm_count(), &t);
+  int st = build_tiling(p->cache, p->hq, n_rows, kinds, seq, off, max_pages, device_sm_count(), p->window, &t);
   if (st != MIXATTN_OK) return st;
   // the previous run may still be copying from the pinned buffer
   if (p->copy_recorded) {
@@ -342,6 +419,7 @@ int mixattn_kv_append_quant(const mixattn_kv_cache* cache, const void* k_new, co
   if (n_new == 0) return MIXATTN_OK;
   if (!k_new || !v_new || !slot_mapping) return MIXATTN_ERR_INVALID_ARG;
   if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 4)) return MIXATTN_ERR_INVALID_ARG;
+  if ((st = pending_device_check()) != MIXATTN_OK) return st;
   unsigned int* err = error_word();
   if (!err) return MIXATTN_ERR_CUDA;
   cudaError_t e = launch_kv_append(*cache, k_new, v_new, slot_mapping, n_new, err,
@@ -356,6 +434,7 @@ int mixattn_kv_export_blocks(const mixattn_kv_cache* cache, int32_t which, const
   if ((which != 0 && which != 1) || n < 0) return MIXATTN_ERR_INVALID_ARG;
   if (n == 0) return MIXATTN_OK;
   if (!slots || !out || !aligned(slots, 4)) return MIXATTN_ERR_INVALID_ARG;
+  if ((st = pending_device_check()) != MIXATTN_OK) return st;
   unsigned int* err = error_word();
   if (!err) return MIXATTN_ERR_CUDA;
   cudaError_t e = launch_kv_export(*cache, which, slots, n, out, err, static_cast<cudaStream_t>(stream));
@@ -365,13 +444,23 @@ int mixattn_kv_export_blocks(const mixattn_kv_cache* cache, int32_t which, const
 int mixattn_plan_create(mixattn_plan** plan_out, const mixattn_kv_cache* cache, int32_t num_q_heads,
                         int32_t n_rows, const int32_t* row_kinds, const int32_t* seq_lens,
                         const int32_t* q_offsets, int32_t max_pages, size_t* workspace_bytes) {
+  return mixattn_plan_create_window(plan_out, cache, num_q_heads, 0, n_rows, row_kinds, seq_lens, q_offsets,
+                                    max_pages, workspace_bytes);
+}
+
+int mixattn_plan_create_window(mixattn_plan** plan_out, const mixattn_kv_cache* cache, int32_t num_q_heads,
+                               int32_t window, int32_t n_rows, const int32_t* row_kinds, const int32_t* seq_lens,
+                               const int32_t* q_offsets, int32_t max_pages, size_t* workspace_bytes) {
   if (!plan_out) return MIXATTN_ERR_INVALID_ARG;
   *plan_out = nullptr;
   int st = check_cache(cache);
   if (st != MIXATTN_OK) return st;
   if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return MIXATTN_ERR_INVALID_ARG;
+  if (window < 0) return MIXATTN_ERR_INVALID_ARG;
+  arm_device_check();
   mixattn_plan* p = new mixattn_plan();
   p->cache = *cache;
+  p->window = window;
   p->hq = num_q_heads;
   p->group = num_q_heads / cache->num_kv_heads;
   p->log2_group = 0;
@@ -417,6 +506,7 @@ int mixattn_run(const mixattn_plan* plan_c, const void* q, const int32_t* page_t
   if (!aligned(q, 16) || !aligned(o, 16) || !aligned(page_table, 4)) return MIXATTN_ERR_INVALID_ARG;
   const WorkspaceLayout& L = plan->tiling.L;
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return MIXATTN_ERR_WORKSPACE;
+  if (int st = pending_device_check()) return st;
   unsigned int* err = error_word();
   if (!err) return MIXATTN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -448,7 +538,7 @@ int mixattn_run(const mixattn_plan* plan_c, const void* q, const int32_t* page_t
   p.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
   p.partials = reinterpret_cast<float*>(ws + L.partials);
   p.chunk_partials = reinterpret_cast<float*>(ws + L.chunk_partials);
-  p.chunk_counters = p.counters + (size_t)plan->n_rows * c.num_kv_heads;
+  p.chunk_counters = p.counters + plan->tiling.n_decode;
   p.max_pages = plan->max_pages;
   p.num_pages = c.num_pages;
   p.n_chunk_tiles = plan->tiling.n_chunk;
@@ -459,6 +549,8 @@ int mixattn_run(const mixattn_plan* plan_c, const void* q, const int32_t* page_t
   p.group = plan->group;
   p.log2_group = plan->log2_group;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
+  p.window = plan->window;
+  p.slot_rows = plan->tiling.slot_rows;
   cudaError_t e = dispatch_attention(c.k_fmt, c.v_fmt, c.head_dim, p, err, s);
   return e == cudaSuccess ? MIXATTN_OK : MIXATTN_ERR_CUDA;
 }
@@ -478,7 +570,8 @@ int mixattn_workspace_bytes(const mixattn_kv_cache* cache, int32_t num_q_heads, 
   if (st != MIXATTN_OK) return st;
   if (!workspace_bytes) return MIXATTN_ERR_INVALID_ARG;
   Tiling t;
-  st = build_tiling(*cache, num_q_heads, n_rows, row_kinds, seq_lens, q_offsets, max_pages, device_sm_count(), &t);
+  st = build_tiling(*cache, num_q_heads, n_rows, row_kinds, seq_lens, q_offsets, max_pages, device_sm_count(), 0,
+                    &t);
   if (st != MIXATTN_OK) return st;
   *workspace_bytes = t.L.total;
   return MIXATTN_OK;
@@ -503,6 +596,9 @@ int64_t mixattn_device_error(int32_t clear) {
   if (clear) {
     const unsigned int z = 0;
     if (cudaMemcpyToSymbol(g_device_error, &z, sizeof(z)) != cudaSuccess) return MIXATTN_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices && g_err_flag[dev])
+      *g_err_flag[dev] = 0u;
   }
   return (int64_t)v;
 }
@@ -515,6 +611,7 @@ const char* mixattn_status_string(int32_t status) {
     case MIXATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case MIXATTN_ERR_CUDA: return "CUDA runtime error";
     case MIXATTN_ERR_DEVICE_CHECK: return "device-side check failed";
+    case MIXATTN_ERR_CLIENT_QUOTA: return "client quota: too many requests waiting for this client";
     default: return "unknown status";
   }
 }

@@ -32,6 +32,8 @@
 #pragma once
 
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -86,9 +88,9 @@ struct DecodeSmem {
   static constexpr int kFs = kFsK + (FV == MIXATTN_KV_F16 ? 0 : 64 * kNb);
   __host__ __device__ static constexpr int kWarpBytes(int ns) { return ns * kStage + kFs; }
   // after the rings, shared by the tile's warps, [16-byte word j][lane]: the lanes' Q
-  // fragments (D/16 k-steps x 2 words), score-accumulator starts (4 floats) and
-  // one-hot words of the value correction (4)
-  static constexpr int kQBytes = (kNb + 2) * 512;
+  // fragments (D/16 k-steps x 2 words), score-accumulator starts (4 floats),
+  // one-hot words of the value correction (4) and the lane's score scale (1 float)
+  static constexpr int kQBytes = (kNb + 3) * 512;
   __host__ __device__ static constexpr int q_off(int ns) { return kWarps * kWarpBytes(ns); }
   static constexpr int stages_for(int budget) {
     return (budget - kWarps * kFs - kQBytes) / (kWarps * kStage) > 8
@@ -253,10 +255,18 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   const int G = p.group;
   const int g = t.kvh;
   const RowInfo ri = p.rows[t.row];
-  const int n_pages_row = (ri.seq_len + kPage - 1) / kPage;
-  const int ppw = decode_pages_per_warp(n_pages_row);
-  const int pps = kWarps * ppw;
-  const int split = t.begin / pps;
+  const int split = t.part;
+  // The tile's R = nq * G rows are (query, head) pairs: row rr is query qg0 + rr / G of
+  // the row (position q_offset + that) and head rr % G of kv head g.  A decode row has
+  // one query; a short chunk row (speculative verify) has up to 8 / G per tile.
+  const int qg0 = t.kv1, nq = t.nsplit, R = nq * G;
+  const int my_q = qg0 + (r < R ? (r >> p.log2_group) : 0), my_h = r & (G - 1);
+  const int pos = ri.q_offset + my_q;                // this lane's row sees keys lo .. pos
+  const int lo = window_first_key(pos, p.window);    // (a sliding window starts at lo)
+  const int pos_first = ri.q_offset + qg0;           // the group's earliest query
+  const int lo_first = window_first_key(pos_first, p.window);
+  const int lo_last = window_first_key(pos_first + nq - 1, p.window);
+  const int slot_rows = p.slot_rows > 0 ? p.slot_rows : G;  // rows per partial slot
   // the tile's pages spread evenly over its 8 warps (runs differing by at most one
   // page, each at most ppw), so a row's shorter last split also keeps every warp busy
   const int pg_base = t.count / kWarps, pg_rem = t.count - pg_base * kWarps;
@@ -264,7 +274,7 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   const int wp1 = wp0 + pg_base + (warp < pg_rem ? 1 : 0);
   const int n_mt = wp1 > wp0 ? 2 * (wp1 - wp0) : 0;  // the warp's M-tiles (16 keys each)
 
-  // ---- Q as the A operand of S = Q K^T: head r in M row r (rows 8..15 zero) ----
+  // ---- Q as the A operand of S = Q K^T: tile row r in M row r (rows 8..15 zero) ----
   // quantised K: k-step 2b+j covers dims 32b + 16j + 4c + {0, 2} (a0) and {1, 3}
   //   (a2), the order of the subnormal pairs of one K word; for Q4_0 the j = 1
   //   k-step (high nibbles, 16 n) takes q / 16
@@ -273,9 +283,8 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   float o_acc[KS][4];
 #pragma unroll
   for (int i = 0; i < KS; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
-  float corr[4] = {0.f, 0.f, 0.f, 0.f};  // quantised V: row b, heads 2c, 2c+1
-  float m_run = -CUDART_INF_F, l_run = 0.f;  // head r, in log2 units
-  const float sl2 = QK ? p.scale_log2 * kTwo24 : p.scale_log2;
+  float corr[4] = {0.f, 0.f, 0.f, 0.f};  // quantised V: row b, tile rows 2c, 2c+1
+  float m_run = -CUDART_INF_F, l_run = 0.f;  // tile row r, in log2 units
 
   const int32_t* pt_row = p.page_table + (int64_t)t.row * p.max_pages;
   const uint32_t ring_s = smem_u32(smem) + warp * S::kWarpBytes(NS);
@@ -338,10 +347,30 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   const uint32_t q_s = smem_u32(smem) + S::q_off(NS);
   if (warp == 0) {
     uint32_t qa[KS][2];
-    float cb[4] = {0.f, 0.f, 0.f, 0.f};  // start of block b's score accumulator (head r)
-    const bool real = r < G;
+    float cb[4] = {0.f, 0.f, 0.f, 0.f};  // start of block b's score accumulator (tile row r)
+    const bool real = r < R;
     const uint16_t* qrow =
-        static_cast<const uint16_t*>(p.q) + ((int64_t)ri.q_start * p.hq + (int64_t)g * G + (real ? r : 0)) * D;
+        static_cast<const uint16_t*>(p.q) + ((int64_t)(ri.q_start + my_q) * p.hq + (int64_t)g * G + my_h) * D;
+    // Q4_0 K: the high-nibble k-steps take q / 16, which is an fp16 subnormal (and
+    // loses bits) for |q| below ~1e-3.  Each head's query is scaled by a power of two
+    // sigma (exact) that puts its largest element in [1024, 2048); the head's score
+    // scale takes 1 / sigma.  Other formats keep sigma = 1.
+    float sig = 1.f;
+    if (FK == MIXATTN_KV_Q4_0) {
+      float mx = 0.f;
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const uint2 v = ldg_u64(qrow + 32 * b + 16 * j + 4 * c);
+          mx = fmax3(mx, fabsf(h2f_lo(v.x)), fabsf(h2f_hi(v.x)));
+          mx = fmax3(mx, fabsf(h2f_lo(v.y)), fabsf(h2f_hi(v.y)));
+        }
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+      // mx is 0 or an fp16 magnitude (exponent -24 .. 15): sigma = 2^(10 - exponent)
+      if (real && mx > 0.f) sig = __uint_as_float((uint32_t)(137 - (int)((__float_as_uint(mx) >> 23) & 0xFF) + 127) << 23);
+    }
     if (!QK) {
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
@@ -356,6 +385,10 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
         for (int j = 0; j < 2; ++j) {
           uint2 v = ldg_u64(qrow + 32 * b + 16 * j + 4 * c);
           if (!real) v = make_uint2(0u, 0u);
+          if (FK == MIXATTN_KV_Q4_0) {  // q * sigma, exact (a power of two into the normal range)
+            v.x = pack_f16x2(h2f_lo(v.x) * sig, h2f_hi(v.x) * sig);
+            v.y = pack_f16x2(h2f_lo(v.y) * sig, h2f_hi(v.y) * sig);
+          }
           qs += (h2f_lo(v.x) + h2f_hi(v.x)) + (h2f_lo(v.y) + h2f_hi(v.y));
           uint32_t e = prmt(v.x, v.y, 0x5410u), o = prmt(v.x, v.y, 0x7632u);
           if (FK == MIXATTN_KV_Q4_0 && j == 1) {
@@ -378,8 +411,12 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
     const uint32_t off = neg_offset_pair<FV>();
     sts128_s(q_s + 512 * (NB + 1) + 16 * lane,
              make_uint4(r == 0 ? off : 0u, r == 1 ? off : 0u, r == 2 ? off : 0u, r == 3 ? off : 0u));
+    sts32f_s(q_s + 512 * (NB + 2) + 16 * lane, 1.f / sig);  // a power of two: exact
   }
   decode_sync(half);
+  // the lane's score scale (log2 units): 1/sqrt(D), the 2^24 of the subnormal codes
+  // (quantised K) and the head's query scale
+  const float sl2 = (QK ? p.scale_log2 * kTwo24 : p.scale_log2) * lds32f_s(q_s + 512 * (NB + 2) + 16 * lane);
 
   // scale conversion: lanes 0-15 take the K scales of key lane, lanes 16-31 the V scales
   // of key lane - 16, into slot (key & 1) + 2 (key >> 3) of quad (key & 7) / 2
@@ -397,7 +434,9 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
     st_cons = st_cons + 1 == NS ? 0 : st_cons + 1;
     if ((page_ok >> (i >> 1)) & 1u) {
       const int key0 = (wp0 + (i >> 1)) * kPage + 16 * (i & 1);  // first key of the M-tile
-      const bool partial = key0 + 16 > ri.seq_len;
+      // some key of the M-tile lies outside some row's range
+      const bool partial = key0 + 16 > pos_first + 1 || key0 < lo_last;
+      auto seen = [&](int k) { return k <= pos && k >= lo; };  // visible to this lane's row
 
       // ---------------- scales of the M-tile -> fp32, one key per lane ----------------
       if (QK || QV) {
@@ -491,10 +530,10 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
       f2_unpack(s01, s[0], s[1]);
       f2_unpack(s89, s[2], s[3]);
       if (partial) {
-        s[0] = key0 + kv0 < ri.seq_len ? s[0] : -CUDART_INF_F;
-        s[1] = key0 + kv0 + 1 < ri.seq_len ? s[1] : -CUDART_INF_F;
-        s[2] = key0 + kv0 + 8 < ri.seq_len ? s[2] : -CUDART_INF_F;
-        s[3] = key0 + kv0 + 9 < ri.seq_len ? s[3] : -CUDART_INF_F;
+        s[0] = seen(key0 + kv0) ? s[0] : -CUDART_INF_F;
+        s[1] = seen(key0 + kv0 + 1) ? s[1] : -CUDART_INF_F;
+        s[2] = seen(key0 + kv0 + 8) ? s[2] : -CUDART_INF_F;
+        s[3] = seen(key0 + kv0 + 9) ? s[3] : -CUDART_INF_F;
       }
       // The reference m_run (per head, log2 units) follows the running maximum
       // lazily: it moves, and O, corr and l are rescaled, only when a score passes it
@@ -585,9 +624,10 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
         } else {
           // fp16: chunks 4h..4h+3 (8 dims each) are rows 0-7 / 8-15 of M-tiles 2h, 2h+1
           uint32_t mk0 = 0xFFFFFFFFu, mk1 = 0xFFFFFFFFu;
-          if (partial) {  // zero the keys past the row so stale data never reaches the MMA
-            mk0 = (key0 + kv0 < ri.seq_len ? 0x0000FFFFu : 0u) | (key0 + kv0 + 1 < ri.seq_len ? 0xFFFF0000u : 0u);
-            mk1 = (key0 + kv0 + 8 < ri.seq_len ? 0x0000FFFFu : 0u) | (key0 + kv0 + 9 < ri.seq_len ? 0xFFFF0000u : 0u);
+          if (partial) {  // zero the keys no row sees, so stale data never reaches the MMA
+            auto any_row = [&](int k) { return k < ri.seq_len && k >= lo_first; };
+            mk0 = (any_row(key0 + kv0) ? 0x0000FFFFu : 0u) | (any_row(key0 + kv0 + 1) ? 0xFFFF0000u : 0u);
+            mk1 = (any_row(key0 + kv0 + 8) ? 0x0000FFFFu : 0u) | (any_row(key0 + kv0 + 9) ? 0xFFFF0000u : 0u);
           }
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
@@ -625,19 +665,19 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   decode_sync(half);  // the staging rings are no longer needed: reuse them as merge scratch
   float* ws = reinterpret_cast<float*>(smem);
   float* wm = ws + warp * S::kPerWarp;  // m[8], l[8], O[8][D]
-  const int h0 = 2 * c, h1 = 2 * c + 1;
-  if (c == 0 && r < G) {
+  const int h0 = 2 * c, h1 = 2 * c + 1;  // O columns: tile rows 2c, 2c+1
+  if (c == 0 && r < R) {
     wm[r] = m_run;
     wm[8 + r] = l_run;
   }
 #pragma unroll
   for (int tt = 0; tt < KS; ++tt) {
     const int d_lo = pv_row_to_d<FV>(tt, r), d_hi = pv_row_to_d<FV>(tt, r + 8);
-    if (h0 < G) {
+    if (h0 < R) {
       wm[16 + h0 * D + d_lo] = o_acc[tt][0];
       wm[16 + h0 * D + d_hi] = o_acc[tt][2];
     }
-    if (h1 < G) {
+    if (h1 < R) {
       wm[16 + h1 * D + d_lo] = o_acc[tt][1];
       wm[16 + h1 * D + d_hi] = o_acc[tt][3];
     }
@@ -645,10 +685,16 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   decode_sync(half);
 
   // ---------------- merge the 8 warps ----------------
-  const int n_out = G * D;
+  // output of tile row rr: query qg0 + rr / G, head g * G + rr % G
+  auto out_of = [&](int rr) {
+    return static_cast<uint16_t*>(p.o) +
+           ((int64_t)(ri.q_start + qg0 + (rr >> p.log2_group)) * p.hq + (int64_t)g * G + (rr & (G - 1))) * D;
+  };
+  const int n_out = R * D;
   const int n_warps_used = min(kWarps, t.count);
   const bool single = ri.n_splits == 1;
-  float* part = p.partials + (int64_t)(t.kv0 + split) * G * (D + 2);  // t.kv0: slot of split 0
+  // split partial: O [slot_rows][D], then (m, l) [slot_rows][2]; t.kv0 is the slot of split 0
+  float* part = p.partials + (int64_t)(t.kv0 + split) * slot_rows * (D + 2);
   for (int idx = tid; idx < n_out; idx += kThreads) {
     const int h = idx / D, d = idx - h * D;
     float mmax = -CUDART_INF_F;
@@ -661,25 +707,24 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
       osum += sc * x[16 + h * D + d];
     }
     if (single) {
-      uint16_t* dst = static_cast<uint16_t*>(p.o) + ((int64_t)ri.q_start * p.hq + (int64_t)g * G + h) * D + d;
-      *dst = __half_as_ushort(__float2half_rn(osum / lsum));
+      out_of(h)[d] = f16_out(osum / lsum);
     } else {
       part[h * D + d] = osum;
       if (d == 0) {
-        part[G * D + 2 * h] = mmax;
-        part[G * D + 2 * h + 1] = lsum;
+        part[slot_rows * D + 2 * h] = mmax;
+        part[slot_rows * D + 2 * h + 1] = lsum;
       }
     }
   }
   if (single) return;
 
-  // ---------------- last CTA of (row, kv head) merges the splits ----------------
+  // ---------------- the last CTA of the group's splits merges them ----------------
   __threadfence();
   decode_sync(half);
   __shared__ int s_last_of[2];
   int& s_last = s_last_of[half];
   if (tid == 0) {
-    const unsigned prev = atomicAdd(&p.counters[(int64_t)t.row * p.hkv + g], 1u);
+    const unsigned prev = atomicAdd(&p.counters[t.kv0], 1u);  // one ticket per split group
     s_last = (prev == (unsigned)(ri.n_splits - 1));
   }
   decode_sync(half);
@@ -687,23 +732,23 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   __threadfence();
   const int first = t.kv0;
   const int ns = ri.n_splits;
+  const int64_t stride = (int64_t)slot_rows * (D + 2);
   for (int idx = tid; idx < n_out; idx += kThreads) {
     const int h = idx / D, d = idx - h * D;
     float mmax = -CUDART_INF_F;
     for (int s2 = 0; s2 < ns; ++s2) {
-      const float* x = p.partials + (int64_t)(first + s2) * G * (D + 2);
-      mmax = fmaxf(mmax, __ldcg(x + G * D + 2 * h));
+      const float* x = p.partials + (first + s2) * stride;
+      mmax = fmaxf(mmax, __ldcg(x + slot_rows * D + 2 * h));
     }
     float lsum = 0.f, osum = 0.f;
     for (int s2 = 0; s2 < ns; ++s2) {
-      const float* x = p.partials + (int64_t)(first + s2) * G * (D + 2);
-      const float mx = __ldcg(x + G * D + 2 * h);
+      const float* x = p.partials + (first + s2) * stride;
+      const float mx = __ldcg(x + slot_rows * D + 2 * h);
       const float sc = mx == -CUDART_INF_F ? 0.f : ex2(mx - mmax);
-      lsum += sc * __ldcg(x + G * D + 2 * h + 1);
+      lsum += sc * __ldcg(x + slot_rows * D + 2 * h + 1);
       osum += sc * __ldcg(x + h * D + d);
     }
-    uint16_t* dst = static_cast<uint16_t*>(p.o) + ((int64_t)ri.q_start * p.hq + (int64_t)g * G + h) * D + d;
-    *dst = __half_as_ushort(__float2half_rn(osum / lsum));
+    out_of(h)[d] = f16_out(osum / lsum);
   }
 }
 
@@ -721,8 +766,17 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int cc) {
 // hi = fp16(v*s); lo = v*s - hi, which is exact in fp16: v*s has at most
 // 18 significant bits, hi keeps the top 11, and the residual is a multiple of
 // the scale's ulp (>= 2^-24) below 2^8 of them.  So hi + lo == v*s exactly.
+//
+// CLAMP (Q8_0): a block whose largest magnitude is 65504 gets the scale
+// fp16(65504/127) = 516, and 127 * 516 = 65532 rounds to infinity in fp16.
+// hi is then clamped to +-65504 (the largest finite fp16, sign kept, one
+// instruction); lo = 65532 - 65504 = 28 is still exact (a multiple of the
+// scale's ulp, 0.5, far inside the fp16 range), so hi + lo == v*s holds for
+// every code and scale.  Q4_0 needs no clamp: |q - 8| * |d| <= 8 * 8188 = 65504.
+template <bool CLAMP>
 __device__ __forceinline__ void split_hilo(uint32_t v, uint32_t s, uint32_t& hi, uint32_t& lo) {
   hi = hmul2_u32(v, s);
+  if (CLAMP) asm("min.xorsign.abs.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x7BFF7BFFu));
   lo = hfma2_u32(v, s, hneg2_u32(hi));  // the negation folds into the fma
 }
 
@@ -824,10 +878,11 @@ __device__ __forceinline__ void convert_half(const HalfRaw<F, D>& r, uint8_t* __
         u4x4_to_f16x2x2((r.q[i].x >> shift) & 0x0F0F0F0Fu, h0, h1);
         u4x4_to_f16x2x2((r.q[i].y >> shift) & 0x0F0F0F0Fu, h2, h3);
       }
-      split_hilo(h0, sc, hi.x, lo.x);
-      split_hilo(h1, sc, hi.y, lo.y);
-      split_hilo(h2, sc, hi.z, lo.z);
-      split_hilo(h3, sc, hi.w, lo.w);
+      constexpr bool kClamp = F == MIXATTN_KV_Q8_0;
+      split_hilo<kClamp>(h0, sc, hi.x, lo.x);
+      split_hilo<kClamp>(h1, sc, hi.y, lo.y);
+      split_hilo<kClamp>(h2, sc, hi.z, lo.z);
+      split_hilo<kClamp>(h3, sc, hi.w, lo.w);
     }
     *reinterpret_cast<uint4*>(dst_hi + doff + i * Gm::KPI * 128) = hi;
     if (LO) *reinterpret_cast<uint4*>(dst_lo + doff + i * Gm::KPI * 128) = lo;
@@ -1056,6 +1111,7 @@ __device__ __forceinline__ void chunk_cta(const AttnParams& p, int cta, int n_ct
       const int g = t.kvh;
       const bool row_valid = tok < t.count;
       const int pos = ri.q_offset + t.begin + min(tok, t.count - 1);
+      const int lo = window_first_key(pos, p.window);  // the row's first visible key
       const int kv0 = t.kv0, n_kv = t.kv1 - t.kv0;
       float m_run = -CUDART_INF_F, l_run = 0.f;
       for (int j = 0; j < n_kv; ++j) {
@@ -1067,8 +1123,9 @@ __device__ __forceinline__ void chunk_cta(const AttnParams& p, int cta, int n_ct
         ok = mbar_wait(&qk_done[st], ph, err) && ok;
         tc_fence_after();
         const int kbase = (kv0 + j) * kChunkN;
-        // causal mask: only a warp whose tile crosses the diagonal pays for it
-        const bool diag = __any_sync(0xFFFFFFFFu, kbase + kChunkN - 1 > pos);
+        // causal (and window) mask: only a warp whose tile crosses the diagonal (or the
+        // window's start) pays for it
+        const bool diag = __any_sync(0xFFFFFFFFu, kbase + kChunkN - 1 > pos || kbase < lo);
         uint32_t a[32];
         // pass 1: the row max of the tile's 128 scores, 32 at a time
         float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
@@ -1079,7 +1136,7 @@ __device__ __forceinline__ void chunk_cta(const AttnParams& p, int cta, int n_ct
           if (diag) {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-              if (kbase + 32 * c + e > pos) a[e] = ninf;
+              if (kbase + 32 * c + e > pos || kbase + 32 * c + e < lo) a[e] = ninf;
           }
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
@@ -1107,7 +1164,7 @@ __device__ __forceinline__ void chunk_cta(const AttnParams& p, int cta, int n_ct
           if (diag) {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-              if (kbase + 32 * c + e > pos) a[e] = ninf;
+              if (kbase + 32 * c + e > pos || kbase + 32 * c + e < lo) a[e] = ninf;
           }
           uint32_t pk[16];
 #pragma unroll
@@ -1181,7 +1238,7 @@ __device__ __forceinline__ void chunk_cta(const AttnParams& p, int cta, int n_ct
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2)
-            pk[e >> 1] = pack_f16x2(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
+            pk[e >> 1] = pack_f16x2_out(__uint_as_float(v[e]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
           if (row_valid && ok && done) {
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4)
@@ -1240,8 +1297,8 @@ __device__ __forceinline__ void chunk_cta(const AttnParams& p, int cta, int n_ct
             }
             if (row_valid && ok && done)
               *reinterpret_cast<uint4*>(dst + d0) =
-                  make_uint4(pack_f16x2(acc[0] * inv_l, acc[1] * inv_l), pack_f16x2(acc[2] * inv_l, acc[3] * inv_l),
-                             pack_f16x2(acc[4] * inv_l, acc[5] * inv_l), pack_f16x2(acc[6] * inv_l, acc[7] * inv_l));
+                  make_uint4(pack_f16x2_out(acc[0] * inv_l, acc[1] * inv_l), pack_f16x2_out(acc[2] * inv_l, acc[3] * inv_l),
+                             pack_f16x2_out(acc[4] * inv_l, acc[5] * inv_l), pack_f16x2_out(acc[6] * inv_l, acc[7] * inv_l));
           }
         }
       }
@@ -1371,9 +1428,9 @@ constexpr int kPersistMaxKvTiles = 64;
 // SMs of the current device, read once per device (a very large count when it
 // cannot be read: then every chunk tile gets its own CTA).
 inline int sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[kMaxDevices] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1 << 30;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1 << 30;
   if (cached[dev] == 0) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1 << 30;
@@ -1399,14 +1456,25 @@ cudaError_t launch_attention_t(const AttnParams& p, unsigned int* err, cudaStrea
   constexpr int kDec = DS::kTotal;
   constexpr int kFused = FusedSmem<FK, FV, D>::kBytes;
   auto* dec_kernel = decode_attention_kernel<FK, FV, D, DS::kSoloMinBlocks, DS::kSoloStages>;
-  static bool configured = false;  // the attribute is per function, once per process
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(dec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDec);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(mixed_attention_kernel<FK, FV, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kFused);
+  // The shared-memory limit is an attribute of the function in the current
+  // device's context: set it once per device (under a lock, host threads may
+  // launch concurrently).
+  {
+    static std::mutex mu;
+    static bool configured[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    configured = true;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev]) {
+      e = cudaFuncSetAttribute(dec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDec);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mixed_attention_kernel<FK, FV, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kFused);
+      if (e != cudaSuccess) return e;
+      configured[dev] = true;
+    }
   }
   if (p.n_chunk_tiles == 0) {
     dec_kernel<<<p.n_decode_tiles, kThreads, kDec, s>>>(p, err);

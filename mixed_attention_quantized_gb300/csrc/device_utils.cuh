@@ -14,9 +14,16 @@
 
 namespace mixattn {
 
-// The device error word lives in abi.cu; kernels receive its address.
+// The device error block lives in abi.cu; kernels receive its address.  Word 0
+// collects the MIXATTN_DEVERR_* bits; words 2-3 hold the device address of a
+// host-mapped flag (0 until a plan has armed it on this device), which is set
+// too, so the host sees at its next call that a check fired without reading
+// device memory.
 __device__ __forceinline__ void set_device_error(unsigned int* err, unsigned int bits) {
-  if (err) atomicOr(err, bits);
+  if (!err) return;
+  atomicOr(err, bits);
+  unsigned int* flag = *reinterpret_cast<unsigned int* volatile*>(err + 2);
+  if (flag) *reinterpret_cast<volatile unsigned int*>(flag) = 1u;
 }
 
 // ---------------------------------------------------------------------------
@@ -87,6 +94,22 @@ __device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c
 __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+// Output conversions: round to nearest even, saturating at +-65504 instead of
+// overflowing to infinity.  An output is a weighted mean of dequantised values,
+// and a Q8_0 block whose largest element is 65504 dequantises it to 127 * 516 =
+// 65532, which plain rounding would turn into infinity; the saturated 65504 is
+// within the fp16 rounding bound of every finite mean.
+__device__ __forceinline__ uint32_t pack_f16x2_out(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+__device__ __forceinline__ uint16_t f16_out(float a) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.f16.f32 %0, %1;" : "=h"(r) : "f"(a));
   return r;
 }
 
@@ -247,6 +270,11 @@ __device__ __forceinline__ uint4 lds128_s(uint32_t a) {
 }
 __device__ __forceinline__ void sts128_s(uint32_t a, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ float lds32f_s(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
 }
 __device__ __forceinline__ void sts32f_s(uint32_t a, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");

@@ -29,6 +29,9 @@ constexpr int kChunkM = 128;       // rows (query tokens x group heads) of a chu
 constexpr int kChunkN = 128;       // keys per KV tile of the chunk path (4 pages)
 constexpr int kPagesPerKvTile = kChunkN / kPage;
 constexpr int kMaxGroup = 8;       // q heads per kv head held in one mma N=8 tile
+constexpr int kMaxDevices = 64;    // per-device caches of the host side (device ordinals below this)
+constexpr int kVerifyMaxRows = 64; // a chunk row with q_len * G <= this (speculative verify) runs on
+                                   // decode-style split-K tiles of up to 8 (query, head) rows
 
 // Per-row data the kernel needs (copied with the tile list).
 struct RowInfo {
@@ -43,9 +46,11 @@ struct RowInfo {
 //           against 128-key KV tiles kv0 .. kv1-1; a tile whose key range is cut
 //           into nsplit pieces (part = 0 .. nsplit-1, consecutive in the tile
 //           list) leaves partial results that the last piece to finish merges
-//   decode: pages begin .. begin+count-1 of `row`, kv head kvh; kv0 = partial slot of
-//           the (row, kv head)'s first split (its splits take slots kv0 .. kv0+n_splits-1,
-//           wherever the tiles sit in the list); kv1..nsplit unused
+//   decode: pages begin .. begin+count-1 of `row`, kv head kvh, split `part` of the
+//           row's n_splits, for queries kv1 .. kv1+nsplit-1 of the row (one query for a
+//           decode row; up to 8 / G for a short chunk row); kv0 = partial slot of the
+//           group's first split (its splits take slots kv0 .. kv0+n_splits-1, wherever
+//           the tiles sit in the list), which also indexes the group's split ticket
 struct TileDesc {
   int32_t row;
   int32_t kvh;
@@ -85,26 +90,30 @@ MIXATTN_HD int scale_row_bytes(int fmt, int head_dim) {
 struct WorkspaceLayout {
   size_t rows;            // RowInfo[n_rows]
   size_t tiles;           // TileDesc[n_tiles]      (chunk tiles first)
-  size_t counters;        // uint32[n_rows * Hkv + n_chunk_tiles]  (zeroed by every run's copy):
-                          // decode split tickets per (row, kv head), then chunk-piece tickets
+  size_t counters;        // uint32[n_decode_tiles + n_chunk_tiles]  (zeroed by every run's copy):
+                          // decode split tickets (indexed by a group's first partial slot), then
+                          // chunk-piece tickets
   size_t upload_end;      // end of the block copied from the plan's host buffer
-  size_t partials;        // float[n_decode_tiles][G][head_dim + 2]
+  size_t partials;        // float[n_decode_tiles][slot_rows][head_dim + 2]
   size_t chunk_partials;  // float[n_chunk_tiles][128][head_dim + 2] when any chunk tile is split
   size_t total;
 };
 
 MIXATTN_HD size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-MIXATTN_HD WorkspaceLayout workspace_layout(int n_rows, int n_tiles, int n_decode_tiles, int hkv,
-                                            int group, int head_dim, bool chunk_split) {
+// slot_rows: rows of one decode partial slot, G (every decode-kind tile holds one
+// query) or 8 when the plan has verify groups
+MIXATTN_HD WorkspaceLayout workspace_layout(int n_rows, int n_tiles, int n_decode_tiles, int slot_rows,
+                                            int head_dim, bool chunk_split) {
   const size_t n_chunk = (size_t)(n_tiles - n_decode_tiles);
   WorkspaceLayout L;
   L.rows = 256;
   L.tiles = align_up(L.rows + sizeof(RowInfo) * (size_t)n_rows, 16);
   L.counters = align_up(L.tiles + sizeof(TileDesc) * (size_t)n_tiles, 16);
-  L.upload_end = align_up(L.counters + sizeof(uint32_t) * ((size_t)n_rows * hkv + n_chunk), 16);
+  L.upload_end = align_up(L.counters + sizeof(uint32_t) * ((size_t)n_decode_tiles + n_chunk), 16);
   L.partials = align_up(L.upload_end, 256);
-  L.chunk_partials = align_up(L.partials + sizeof(float) * (size_t)n_decode_tiles * group * (head_dim + 2), 256);
+  L.chunk_partials =
+      align_up(L.partials + sizeof(float) * (size_t)n_decode_tiles * slot_rows * (head_dim + 2), 256);
   L.total = align_up(L.chunk_partials + (chunk_split ? sizeof(float) * n_chunk * kChunkM * (head_dim + 2) : 0), 256);
   return L;
 }
@@ -120,8 +129,8 @@ struct AttnParams {
   const int32_t* page_table;  // [n_rows][max_pages]
   const RowInfo* rows;
   const TileDesc* tiles;
-  uint32_t* counters;         // [n_rows][hkv], then one per chunk tile (piece tickets)
-  float* partials;            // [n_decode_tiles][group][D + 2]
+  uint32_t* counters;         // [n_decode_tiles] split tickets, then one per chunk tile (piece tickets)
+  float* partials;            // [n_decode_tiles][slot_rows][D + 2]
   float* chunk_partials;      // O [n_chunk_tiles][128][D], then (m, l) [n_chunk_tiles][128] of the
                               // pieces of cut chunk tiles
   uint32_t* chunk_counters;   // [n_chunk_tiles]: piece tickets, indexed by a tile's first piece
@@ -136,7 +145,14 @@ struct AttnParams {
   int32_t group;              // hq / hkv, 1..8
   int32_t log2_group;
   float scale_log2;           // log2(e) / sqrt(D)
+  int32_t window = 0;         // > 0: sliding window, the query at position p sees keys p-window+1 .. p
+  int32_t slot_rows = 0;      // rows of a decode partial slot (0: group)
 };
+
+// First key a query at position `pos` sees (0 without a window).
+MIXATTN_HD int window_first_key(int pos, int window) {
+  return (window > 0 && pos + 1 > window) ? pos + 1 - window : 0;
+}
 
 }  // namespace mixattn
 

@@ -118,7 +118,7 @@ int tile_into_upload(const mixattn_kv_cache& c, int hq, int n_rows, const int32_
   const int64_t n_tiles = n_chunk + n_decode;
   if (n_tiles > INT32_MAX / 2) return MIXATTN_ERR_INVALID_ARG;
   // this path never cuts chunk tiles (its scratch holds no chunk partials)
-  const WorkspaceLayout L = workspace_layout(n_rows, (int)n_tiles, (int)n_decode, hkv, G, c.head_dim, false);
+  const WorkspaceLayout L = workspace_layout(n_rows, (int)n_tiles, (int)n_decode, G, c.head_dim, false);
   if (L.total > kStaticScratchBytes || L.upload_end - L.rows > kStaticUploadBytes) return MIXATTN_ERR_WORKSPACE;
 
   // second pass: write the image
@@ -150,7 +150,8 @@ int tile_into_upload(const mixattn_kv_cache& c, int hq, int n_rows, const int32_
         const int32_t first = (int32_t)(id - n_chunk);  // partial slot of split 0
         for (int sp = 0; sp < ns; ++sp)
           tiles[id++] =
-              TileDesc{r, g, sp * pps, (int32_t)std::min<int64_t>(pps, n_pages - (int64_t)sp * pps), first, 0, 0, 1};
+              TileDesc{r, g, sp * pps, (int32_t)std::min<int64_t>(pps, n_pages - (int64_t)sp * pps), first, 0, sp, 1};
+        // (kv1 = 0, nsplit = 1: the group is the decode row's one query)
       }
     }
     q0 += nq;
@@ -227,7 +228,7 @@ extern "C" int mixattn_mixed_attention_noalloc(const mixattn_kv_cache* cache, in
   p.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
   p.partials = reinterpret_cast<float*>(ws + L.partials);
   p.chunk_partials = reinterpret_cast<float*>(ws + L.chunk_partials);
-  p.chunk_counters = p.counters + (size_t)n_rows * cache->num_kv_heads;
+  p.chunk_counters = p.counters + n_decode;
   p.max_pages = max_pages;
   p.num_pages = cache->num_pages;
   p.n_chunk_tiles = n_chunk;

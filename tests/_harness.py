@@ -32,10 +32,10 @@ def build_cache(w: wl.Workload, fill: int = 0, append_tokens: int = 32768, pt=No
     return cache, pt
 
 
-def run_attention(w: wl.Workload, cache, pt, q=None):
+def run_attention(w: wl.Workload, cache, pt, q=None, window: int = 0):
     t = torch()
     import mixed_attention_quantized_gb300 as mq
-    plan = mq.Plan(cache, w.num_q_heads, w.row_kinds, w.seq_lens, w.q_offsets, pt.shape[1])
+    plan = mq.Plan(cache, w.num_q_heads, w.row_kinds, w.seq_lens, w.q_offsets, pt.shape[1], window=window)
     ws = mq.alloc_workspace(plan.workspace_bytes)
     qd = t.from_numpy(wl.queries(w)).cuda() if q is None else q
     o = t.full_like(qd, float("nan"))
@@ -45,7 +45,7 @@ def run_attention(w: wl.Workload, cache, pt, q=None):
     return o.cpu().numpy()
 
 
-def oracle_attention(w: wl.Workload, sel=None, threads: int = 0) -> np.ndarray:
+def oracle_attention(w: wl.Workload, sel=None, threads: int = 0, window: int = 0) -> np.ndarray:
     """fp64 oracle for the packed query indices `sel` (default: all)."""
     total = w.total_q
     sel = np.arange(total) if sel is None else np.asarray(sel)
@@ -67,7 +67,7 @@ def oracle_attention(w: wl.Workload, sel=None, threads: int = 0) -> np.ndarray:
         acc += w.q_lens[r]
     q = np.concatenate(qs, axis=0)
     sub_sel = np.array([new_index[r] + (s - w.q_starts[r]) for s, r in zip(sel, row_of)], dtype=np.int32)
-    return oracle.attention(w.k_fmt, w.v_fmt, q, kb, vb, seq, off, sel=sub_sel, threads=threads)
+    return oracle.attention(w.k_fmt, w.v_fmt, q, kb, vb, seq, off, sel=sub_sel, threads=threads, window=window)
 
 
 def max_err(gpu: np.ndarray, ref: np.ndarray) -> float:

@@ -102,10 +102,21 @@ def test_bad_page_id_sets_the_device_error():
     bad[0, 1] = w.num_pages + 5
     bad[1, 0] = -3
     out = run_attention(w, cache, bad)
-    assert mq.device_error(clear=True) & mq.DEVERR_PAGE_ID
-    # the error is reported; the good pages still produced numbers of the right shape
+    # the good pages still produced numbers of the right shape
     assert out.shape == (w.total_q, 8, 64)
+    # the next call sees that a device check fired and launches nothing
+    with pytest.raises(mq.MixattnError) as e:
+        run_attention(w, cache, pt)
+    assert e.value.status == mq.ERR_DEVICE_CHECK
+    with pytest.raises(mq.MixattnError) as e:
+        k, v = wl.row_kv(w, 0, 0, 1)
+        mq.kv_append_quant(cache, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(),
+                           torch.zeros(1, dtype=torch.int32, device="cuda"))
+    assert e.value.status == mq.ERR_DEVICE_CHECK
+    assert mq.device_error(clear=True) & mq.DEVERR_PAGE_ID
     assert mq.device_error(clear=True) == 0
+    # cleared: calls run again
+    assert max_err(run_attention(w, cache, pt), oracle_attention(w)) <= TOL
 
 
 def test_one_call_entry_point_matches_the_plan_path():
@@ -196,3 +207,64 @@ def test_values_near_the_fp16_limit_stay_finite(kf, vf):
     assert np.isfinite(out).all()
     assert (np.abs(out - ref) <= TOL * gain + np.abs(ref) * 2.0 ** -11).all(), np.abs(out - ref).max()
 
+
+
+LIMIT_PAIRS = [(wl.FMT_Q8_0, wl.FMT_Q8_0), (wl.FMT_Q8_0, wl.FMT_Q4_0), (wl.FMT_Q4_0, wl.FMT_Q8_0),
+               (wl.FMT_Q4_0, wl.FMT_Q4_0)]
+LIMIT_GAIN = 30000.0  # ~3% of the values clip at +-65504: most blocks hold the largest fp16 value
+
+
+def _limit_workload(kf, vf, which, rows, seed=23):
+    # K at the limit: queries scaled by 1e-4 keep the scores O(1) (K x 3e4 x Q x 1e-4),
+    # so the fp32 accumulation of scores stays far inside the budget; unscaled, scores of
+    # ~1e4 carry fp32 rounding of ~1e-3 each, which the softmax turns into output errors
+    # of ~1e-2 on any fp32-accumulating implementation
+    gains = {"k_gain": LIMIT_GAIN, "q_gain": 1e-4} if which == "k" else {"v_gain": LIMIT_GAIN}
+    return wl.custom(f"limit_{which}", 32, 8, 128, kf, vf, seed, rows, **gains)
+
+
+def _limit_bound(which, ref):
+    """Errors scale with the values: the 2e-3 budget per unit of V (V at the limit),
+    plus the fp16 rounding of the output itself (saturating at 65504)."""
+    return TOL * (LIMIT_GAIN if which == "v" else 1.0) + np.abs(ref) * 2.0 ** -11
+
+
+@pytest.mark.parametrize("kf,vf", LIMIT_PAIRS)
+@pytest.mark.parametrize("which", ["k", "v"])
+def test_blocks_holding_the_largest_fp16_value_match_oracle(kf, vf, which):
+    """K or V blocks whose largest element is +-65504: a Q8_0 scale of 516 and a
+    dequantised 127 * 516 = 65532, beyond the fp16 range, in decode rows and in
+    chunk rows (the chunk path splits every value into fp16 halves, whose high
+    half must not overflow).  Every output is finite and within the oracle's
+    value-scaled bound."""
+    rows = [(D, 3000, 2999), (D, 700, 699), (D, 33, 32), (C, 300, 200), (C, 129, 0)]
+    w = _limit_workload(kf, vf, which, rows)
+    k, v = wl.row_kv(w, 0)
+    x = (k if which == "k" else v).astype(np.float32)
+    assert (np.abs(x) == wl.FP16_MAX).any()  # the inputs do reach the limit
+    cache, pt = build_cache(w)
+    out = run_attention(w, cache, pt).astype(np.float64)
+    ref = oracle_attention(w)
+    assert np.isfinite(out).all()
+    err = np.abs(out - ref)
+    assert (err <= _limit_bound(which, ref)).all(), err.max()
+
+
+@pytest.mark.parametrize("kf,vf", [(wl.FMT_Q8_0, wl.FMT_Q8_0), (wl.FMT_Q8_0, wl.FMT_Q4_0), (wl.FMT_Q4_0, wl.FMT_Q8_0)])
+@pytest.mark.parametrize("which", ["k", "v"])
+def test_decode_row_matches_last_chunk_row_at_the_fp16_limit(kf, vf, which):
+    """The invariant a decode row == the last row of the same sequence run as a
+    chunk, on blocks holding +-65504 (decode tiles keep scales in fp32; chunk
+    tiles use the fp16 hi/lo split)."""
+    import torch
+    wc = _limit_workload(kf, vf, which, [(C, 3000, 2000)], seed=29)
+    wd = _limit_workload(kf, vf, which, [(D, 3000, 2999)], seed=29)
+    cache, pt = build_cache(wc)
+    oc = run_attention(wc, cache, pt).astype(np.float64)
+    qd = torch.from_numpy(wl.row_q(wc, 0)[-1:].copy()).cuda()
+    od = run_attention(wd, cache, pt, q=qd).astype(np.float64)
+    assert np.isfinite(oc).all() and np.isfinite(od).all()
+    ref = oracle_attention(wc, sel=[999])
+    bound = _limit_bound(which, ref)
+    assert (np.abs(od - ref) <= bound).all() and (np.abs(oc[-1:] - ref) <= bound).all()
+    assert (np.abs(oc[-1:] - od) <= 2 * bound).all()

@@ -32,6 +32,7 @@ ROW_DECODE, ROW_CHUNK = 0, 1
 FMT_NAMES = {FMT_F16: "f16", FMT_Q8_0: "q8_0", FMT_Q4_0: "q4_0"}
 TOKEN_BLOCK = 4096
 PAGE = 32
+FP16_MAX = 65504.0  # largest finite fp16 value
 
 # tensor ids for the seed sequences
 _T_K, _T_V, _T_Q, _T_OUTLIER, _T_ROWS, _T_PAGES = 1, 2, 3, 4, 5, 6
@@ -53,8 +54,9 @@ class Workload:
     alpha: float = 8.0
     page_size: int = PAGE
     spare_pages: int = 0
-    v_gain: float = 1.0  # V values multiplied by this (then kept inside +-60000)
+    v_gain: float = 1.0  # V values multiplied by this (then clipped to the fp16 range, +-65504)
     q_gain: float = 1.0  # queries multiplied by this (sharper scores)
+    k_gain: float = 1.0  # K values multiplied by this (then clipped to the fp16 range)
 
     @property
     def n_rows(self) -> int:
@@ -106,7 +108,7 @@ def _normal_f16(key: Tuple[int, ...], shape, scale_cols=None, gain: float = 1.0)
     if scale_cols is not None:
         x = x * scale_cols
     if gain != 1.0:
-        x = np.clip(x * np.float32(gain), -60000.0, 60000.0)
+        x = np.clip(x * np.float32(gain), -FP16_MAX, FP16_MAX)
     return x.astype(np.float16)
 
 
@@ -131,7 +133,7 @@ def row_kv(w: Workload, r: int, start: int = 0, stop: Optional[int] = None):
         cols = np.ones(shape, dtype=np.float32)
         for g, chans in enumerate(outlier_channels(w)):
             cols[g, chans] = np.float32(w.alpha)
-    k = _blocked(w, r, _T_K, start, stop, shape, cols)
+    k = _blocked(w, r, _T_K, start, stop, shape, cols, gain=w.k_gain)
     v = _blocked(w, r, _T_V, start, stop, shape, gain=w.v_gain)
     return k, v
 
@@ -213,19 +215,21 @@ def fairness(k_fmt: int = FMT_Q4_0, v_fmt: Optional[int] = None, offset: int = 2
                     q_offsets=[s - 1 for s in seq[:-1]] + [offset])
 
 
-def decode_sweep(batch: int, ctx: int, fmt: int) -> Workload:
-    """``batch`` decode rows all at ``ctx``, 32 q / 8 kv heads, D 128."""
+def decode_sweep(batch: int, ctx: int, fmt: int, v_fmt: Optional[int] = None) -> Workload:
+    """``batch`` decode rows all at ``ctx``, 32 q / 8 kv heads, D 128 (K format
+    ``fmt``; V format ``v_fmt``, default the same)."""
     idx = {1: 0, 4: 1, 16: 2, 64: 3}.get(batch, 4) * 2 + (0 if ctx <= 8192 else 1)
     seed = 4000 + idx
-    return Workload(f"decode_sweep_b{batch}_ctx{ctx}", 32, 8, 128, fmt, fmt, seed,
+    return Workload(f"decode_sweep_b{batch}_ctx{ctx}", 32, 8, 128, fmt, fmt if v_fmt is None else v_fmt, seed,
                     row_kinds=[ROW_DECODE] * batch, seq_lens=[ctx] * batch,
                     q_offsets=[ctx - 1] * batch)
 
 
 def custom(name: str, hq: int, hkv: int, d: int, k_fmt: int, v_fmt: int, seed: int,
            rows: List[Tuple[int, int, int]], n_outlier: int = 0, alpha: float = 8.0,
-           spare_pages: int = 0, v_gain: float = 1.0, q_gain: float = 1.0) -> Workload:
+           spare_pages: int = 0, v_gain: float = 1.0, q_gain: float = 1.0,
+           k_gain: float = 1.0) -> Workload:
     """Free-form workload; rows are (kind, seq_len, q_offset)."""
     return Workload(name, hq, hkv, d, k_fmt, v_fmt, seed, [r[0] for r in rows],
                     [r[1] for r in rows], [r[2] for r in rows], n_outlier, alpha,
-                    spare_pages=spare_pages, v_gain=v_gain, q_gain=q_gain)
+                    spare_pages=spare_pages, v_gain=v_gain, q_gain=q_gain, k_gain=k_gain)
