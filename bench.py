@@ -51,6 +51,10 @@ def make_workload(name: str) -> wl.Workload:
         return wl.long_session(wl.FMT_Q4_0)
     if name == "fairness":
         return wl.fairness()
+    if name == "verify_q8":
+        return wl.verify_batch(wl.FMT_Q8_0)
+    if name == "verify_q4":
+        return wl.verify_batch(wl.FMT_Q4_0)
     if name.startswith("sweep_"):  # sweep_<batch>_<ctx>_<f16|q8_0|q4_0|k8v4|k4v8>
         _, b, c, f = name.split("_", 3)
         mixed = {"k8v4": (wl.FMT_Q8_0, wl.FMT_Q4_0), "k4v8": (wl.FMT_Q4_0, wl.FMT_Q8_0)}
@@ -63,9 +67,10 @@ def make_workload(name: str) -> wl.Workload:
 
 # The other KV formats of the metric, measured after the headline workload by a
 # default run (one sub-object each): the tensor-bound fairness chunk (Q4_0), the
-# long session in both formats, and one fp16 and one K8V4 decode-sweep point.
+# long session in both formats, one fp16 and one K8V4 decode-sweep point, and a
+# batch of speculative-verify rows (Q8_0).
 FORMAT_WORKLOADS = [("fairness", 10), ("long_session_q8", 50), ("long_session_q4", 50),
-                    ("sweep_4_65536_f16", 50), ("sweep_16_8192_k8v4", 50)]
+                    ("sweep_4_65536_f16", 50), ("sweep_16_8192_k8v4", 50), ("verify_q8", 50)]
 
 
 # --------------------------------------------------------------------------

@@ -265,19 +265,23 @@ int build_tiling(const mixattn_kv_cache& c, int hq, int n_rows, const int32_t* k
       const int pps = decode_pages_per_split((int)n_win);
       const int ns = (int)((n_win + pps - 1) / pps);
       rows[r].n_splits = ns;
+      // query groups innermost: the groups reading the same pages sit side by side in
+      // the tile list (and so run at about the same time), and the pages they share
+      // come from L2 after the first read; slots are numbered group-major
+      const int64_t n_groups = (nq + QPG - 1) / QPG;
       for (int g = 0; g < hkv; ++g) {
-        for (int64_t qg = 0; qg < nq; qg += QPG) {
-          const int32_t first = (int32_t)decodes.size();  // partial slot of split 0
-          for (int sp = 0; sp < ns; ++sp) {
+        const int32_t base = (int32_t)decodes.size();
+        for (int sp = 0; sp < ns; ++sp) {
+          for (int64_t gi = 0; gi < n_groups; ++gi) {
             TileDesc t;
             t.row = r;
             t.kvh = g;
             t.begin = (int32_t)(first_page + (int64_t)sp * pps);
             t.count = (int32_t)std::min<int64_t>(pps, n_win - (int64_t)sp * pps);
-            t.kv0 = first;
-            t.kv1 = (int32_t)qg;                                  // the group's first query
+            t.kv0 = base + (int32_t)(gi * ns);                            // partial slot of split 0
+            t.kv1 = (int32_t)(gi * QPG);                                  // the group's first query
             t.part = sp;
-            t.nsplit = (int32_t)std::min<int64_t>(QPG, nq - qg);  // the group's queries
+            t.nsplit = (int32_t)std::min<int64_t>(QPG, nq - gi * QPG);  // the group's queries
             decodes.push_back(t);
           }
         }

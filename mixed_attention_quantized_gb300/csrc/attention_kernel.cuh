@@ -89,7 +89,7 @@ struct DecodeSmem {
   __host__ __device__ static constexpr int kWarpBytes(int ns) { return ns * kStage + kFs; }
   // after the rings, shared by the tile's warps, [16-byte word j][lane]: the lanes' Q
   // fragments (D/16 k-steps x 2 words), score-accumulator starts (4 floats),
-  // one-hot words of the value correction (4) and the lane's score scale (1 float)
+  // one-hot words of the value correction (4) and the K-scale multiplier (1 float)
   static constexpr int kQBytes = (kNb + 3) * 512;
   __host__ __device__ static constexpr int q_off(int ns) { return kWarps * kWarpBytes(ns); }
   static constexpr int stages_for(int budget) {
@@ -263,10 +263,10 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   const int my_q = qg0 + (r < R ? (r >> p.log2_group) : 0), my_h = r & (G - 1);
   const int pos = ri.q_offset + my_q;                // this lane's row sees keys lo .. pos
   const int lo = window_first_key(pos, p.window);    // (a sliding window starts at lo)
-  const int pos_first = ri.q_offset + qg0;           // the group's earliest query
-  const int lo_first = window_first_key(pos_first, p.window);
-  const int lo_last = window_first_key(pos_first + nq - 1, p.window);
-  const int slot_rows = p.slot_rows > 0 ? p.slot_rows : G;  // rows per partial slot
+  // an M-tile needs masks when it reaches past the group's earliest query or
+  // before its latest window start (the same bounds for every lane)
+  const int mask_hi = ri.q_offset + qg0 + 1;
+  const int mask_lo = window_first_key(ri.q_offset + qg0 + nq - 1, p.window);
   // the tile's pages spread evenly over its 8 warps (runs differing by at most one
   // page, each at most ppw), so a row's shorter last split also keeps every warp busy
   const int pg_base = t.count / kWarps, pg_rem = t.count - pg_base * kWarps;
@@ -277,7 +277,7 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   // ---- Q as the A operand of S = Q K^T: tile row r in M row r (rows 8..15 zero) ----
   // quantised K: k-step 2b+j covers dims 32b + 16j + 4c + {0, 2} (a0) and {1, 3}
   //   (a2), the order of the subnormal pairs of one K word; for Q4_0 the j = 1
-  //   k-step (high nibbles, 16 n) takes q / 16
+  //   k-step (high nibbles, 16 n) takes q * sigma / 16 (see below)
   // fp16 K: k-step ks covers dims 16ks + 2c + {0, 1} (a0) and {8, 9} (a2)
 
   float o_acc[KS][4];
@@ -351,25 +351,28 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
     const bool real = r < R;
     const uint16_t* qrow =
         static_cast<const uint16_t*>(p.q) + ((int64_t)(ri.q_start + my_q) * p.hq + (int64_t)g * G + my_h) * D;
-    // Q4_0 K: the high-nibble k-steps take q / 16, which is an fp16 subnormal (and
-    // loses bits) for |q| below ~1e-3.  Each head's query is scaled by a power of two
-    // sigma (exact) that puts its largest element in [1024, 2048); the head's score
-    // scale takes 1 / sigma.  Other formats keep sigma = 1.
+    // Q4_0 K: the high-nibble k-steps take q / 16, an fp16 subnormal (losing bits) for
+    // |q| below ~1e-3.  The tile's queries are scaled by one power of two sigma (exact)
+    // that puts their largest element in [1024, 2048); 1 / sigma joins the K scales
+    // when they are converted to fp32 (below), so the loop pays four multiplies per
+    // 16 keys.  Other formats keep sigma = 1.
     float sig = 1.f;
     if (FK == MIXATTN_KV_Q4_0) {
       float mx = 0.f;
+      if (real) {
 #pragma unroll
-      for (int b = 0; b < NB; ++b)
+        for (int b = 0; b < NB; ++b)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const uint2 v = ldg_u64(qrow + 32 * b + 16 * j + 4 * c);
-          mx = fmax3(mx, fabsf(h2f_lo(v.x)), fabsf(h2f_hi(v.x)));
-          mx = fmax3(mx, fabsf(h2f_lo(v.y)), fabsf(h2f_hi(v.y)));
-        }
-      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+          for (int j = 0; j < 2; ++j) {
+            const uint2 v = ldg_u64(qrow + 32 * b + 16 * j + 4 * c);
+            mx = fmax3(mx, fabsf(h2f_lo(v.x)), fabsf(h2f_hi(v.x)));
+            mx = fmax3(mx, fabsf(h2f_lo(v.y)), fabsf(h2f_hi(v.y)));
+          }
+      }
+#pragma unroll
+      for (int sh = 1; sh < 32; sh <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, sh));
       // mx is 0 or an fp16 magnitude (exponent -24 .. 15): sigma = 2^(10 - exponent)
-      if (real && mx > 0.f) sig = __uint_as_float((uint32_t)(137 - (int)((__float_as_uint(mx) >> 23) & 0xFF) + 127) << 23);
+      if (mx > 0.f) sig = __uint_as_float((uint32_t)(264 - (int)((__float_as_uint(mx) >> 23) & 0xFF)) << 23);
     }
     if (!QK) {
 #pragma unroll
@@ -411,12 +414,12 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
     const uint32_t off = neg_offset_pair<FV>();
     sts128_s(q_s + 512 * (NB + 1) + 16 * lane,
              make_uint4(r == 0 ? off : 0u, r == 1 ? off : 0u, r == 2 ? off : 0u, r == 3 ? off : 0u));
-    sts32f_s(q_s + 512 * (NB + 2) + 16 * lane, 1.f / sig);  // a power of two: exact
+    if (FK == MIXATTN_KV_Q4_0 && lane == 0) sts32f_s(q_s + 512 * (NB + 2), 1.f / sig);  // a power of two: exact
   }
   decode_sync(half);
-  // the lane's score scale (log2 units): 1/sqrt(D), the 2^24 of the subnormal codes
-  // (quantised K) and the head's query scale
-  const float sl2 = (QK ? p.scale_log2 * kTwo24 : p.scale_log2) * lds32f_s(q_s + 512 * (NB + 2) + 16 * lane);
+
+  // score scale (log2 units): 1/sqrt(D) and, for quantised K, the 2^24 of the subnormal codes
+  const float sl2 = QK ? p.scale_log2 * kTwo24 : p.scale_log2;
 
   // scale conversion: lanes 0-15 take the K scales of key lane, lanes 16-31 the V scales
   // of key lane - 16, into slot (key & 1) + 2 (key >> 3) of quad (key & 7) / 2
@@ -435,7 +438,7 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
     if ((page_ok >> (i >> 1)) & 1u) {
       const int key0 = (wp0 + (i >> 1)) * kPage + 16 * (i & 1);  // first key of the M-tile
       // some key of the M-tile lies outside some row's range
-      const bool partial = key0 + 16 > pos_first + 1 || key0 < lo_last;
+      const bool partial = key0 + 16 > mask_hi || key0 < mask_lo;
       auto seen = [&](int k) { return k <= pos && k >= lo; };  // visible to this lane's row
 
       // ---------------- scales of the M-tile -> fp32, one key per lane ----------------
@@ -443,16 +446,19 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
         if (sc_lane) {
           const uint32_t src = st_s + sc_src;
           const uint32_t dst = sc_dst;
+          // multiplier of the converted scales: 1 / sigma for Q4_0 K, else 1 (read here, not
+          // kept in a register across the loop)
+          const float sc_mul = (FK == MIXATTN_KV_Q4_0 && lane < 16) ? lds32f_s(q_s + 512 * (NB + 2)) : 1.f;
           if (NB == 4) {
             const uint2 x = lds64_s(src);
-            sts32f_s(dst, h2f_lo(x.x));
-            sts32f_s(dst + 64, h2f_hi(x.x));
-            sts32f_s(dst + 128, h2f_lo(x.y));
-            sts32f_s(dst + 192, h2f_hi(x.y));
+            sts32f_s(dst, h2f_lo(x.x) * sc_mul);
+            sts32f_s(dst + 64, h2f_hi(x.x) * sc_mul);
+            sts32f_s(dst + 128, h2f_lo(x.y) * sc_mul);
+            sts32f_s(dst + 192, h2f_hi(x.y) * sc_mul);
           } else {
             const uint32_t x = lds32_s(src);
-            sts32f_s(dst, h2f_lo(x));
-            sts32f_s(dst + 64, h2f_hi(x));
+            sts32f_s(dst, h2f_lo(x) * sc_mul);
+            sts32f_s(dst + 64, h2f_hi(x) * sc_mul);
           }
         }
         __syncwarp();
@@ -625,6 +631,7 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
           // fp16: chunks 4h..4h+3 (8 dims each) are rows 0-7 / 8-15 of M-tiles 2h, 2h+1
           uint32_t mk0 = 0xFFFFFFFFu, mk1 = 0xFFFFFFFFu;
           if (partial) {  // zero the keys no row sees, so stale data never reaches the MMA
+            const int lo_first = window_first_key(ri.q_offset + qg0, p.window);
             auto any_row = [&](int k) { return k < ri.seq_len && k >= lo_first; };
             mk0 = (any_row(key0 + kv0) ? 0x0000FFFFu : 0u) | (any_row(key0 + kv0 + 1) ? 0xFFFF0000u : 0u);
             mk1 = (any_row(key0 + kv0 + 8) ? 0x0000FFFFu : 0u) | (any_row(key0 + kv0 + 9) ? 0xFFFF0000u : 0u);
@@ -693,6 +700,7 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const TileDesc&
   const int n_out = R * D;
   const int n_warps_used = min(kWarps, t.count);
   const bool single = ri.n_splits == 1;
+  const int slot_rows = p.slot_rows > 0 ? p.slot_rows : G;  // rows per partial slot
   // split partial: O [slot_rows][D], then (m, l) [slot_rows][2]; t.kv0 is the slot of split 0
   float* part = p.partials + (int64_t)(t.kv0 + split) * slot_rows * (D + 2);
   for (int idx = tid; idx < n_out; idx += kThreads) {
@@ -1101,10 +1109,14 @@ __device__ __forceinline__ void chunk_cta(const AttnParams& p, int cta, int n_ct
       while (k < n_rounds && chunk_tile_of(cta, k, n_ctas, p.n_chunk_tiles) < 0) ++k;
       return k;
     };
+    // Every branch of this group that leads to a named barrier is taken by all of its
+    // 128 threads: the abort flag, which other roles may set at any time, is read
+    // through a group vote (bar_any) wherever a barrier follows, never thread by thread.
+    auto group_abort = [&]() { return bar_any(kBarSoftmax, kGroup, *abort_flag != 0); };
     int k = next_round(0);
     if (k < n_rounds) write_q(chunk_tile_of(cta, k, n_ctas, p.n_chunk_tiles));
     int jg0 = 0;
-    for (; k < n_rounds && !*abort_flag; k = next_round(k + 1)) {
+    for (; k < n_rounds && !group_abort(); k = next_round(k + 1)) {
       const int idx = chunk_tile_of(cta, k, n_ctas, p.n_chunk_tiles);
       const TileDesc t = p.tiles[idx];
       const RowInfo ri = p.rows[t.row];
@@ -1220,7 +1232,7 @@ __device__ __forceinline__ void chunk_cta(const AttnParams& p, int cta, int n_ct
       }
       // the next tile's Q: this tile's last QK is done (its scores were read above)
       const int kn = next_round(k + 1);
-      if (kn < n_rounds && !*abort_flag) write_q(chunk_tile_of(cta, kn, n_ctas, p.n_chunk_tiles));
+      if (kn < n_rounds && !group_abort()) write_q(chunk_tile_of(cta, kn, n_ctas, p.n_chunk_tiles));
       // ---- epilogue of this tile, while the MMA warp starts the next ----
       const bool done = !*abort_flag;
       const int jl = jg0 + n_kv - 1;  // the tile's last KV tile

@@ -215,6 +215,18 @@ def fairness(k_fmt: int = FMT_Q4_0, v_fmt: Optional[int] = None, offset: int = 2
                     q_offsets=[s - 1 for s in seq[:-1]] + [offset])
 
 
+def verify_batch(k_fmt: int = FMT_Q8_0, v_fmt: Optional[int] = None, n_rows: int = 16) -> Workload:
+    """Speculative-verify rows: 16 rows of 4..16 draft tokens each (causal, at the
+    end of a context of U[8192, 32768] tokens), 32 q / 8 kv heads, D 128."""
+    seed = 5000
+    rng = _rng(seed, _T_ROWS)
+    ctx = rng.integers(8192, 32768, size=n_rows, endpoint=True)
+    nq = rng.integers(4, 16, size=n_rows, endpoint=True)
+    seq = [int(c) + int(n) for c, n in zip(ctx, nq)]
+    return Workload("verify", 32, 8, 128, k_fmt, k_fmt if v_fmt is None else v_fmt, seed,
+                    row_kinds=[ROW_CHUNK] * n_rows, seq_lens=seq, q_offsets=[int(c) for c in ctx])
+
+
 def decode_sweep(batch: int, ctx: int, fmt: int, v_fmt: Optional[int] = None) -> Workload:
     """``batch`` decode rows all at ``ctx``, 32 q / 8 kv heads, D 128 (K format
     ``fmt``; V format ``v_fmt``, default the same)."""
