@@ -26,9 +26,9 @@
 // -- an exact hi/lo pair for quantised formats, since d*q needs up to 18
 // significant bits; one thread issues every tcgen05.mma (S = Q K^T and O += P V,
 // one MMA per half, Q, S, P and O in TMEM); a softmax warp group, one TMEM lane
-// (query row) per thread, turns S into P.  K and S are double-buffered and P has
-// its own columns, so QK of the next tile and the dequantisation overlap this
-// tile's softmax and PV.
+// (query row) per thread, turns S into P in place.  K, S and P are double-buffered,
+// so QK of the next tile, the dequantisation and the next softmax overlap this
+// tile's PV.
 #pragma once
 
 #include <algorithm>
@@ -979,10 +979,11 @@ __device__ __forceinline__ int chunk_tile_of(int c, int k, int C, int n) {
 //   V group (warps 8-11): the same for V, into a single buffer, key half h once
 //     the PV MMAs of the previous KV tile that read that half are done;
 //   softmax group (warps 0-3, thread i = TMEM lane i = query row i): reads
-//     S[jg%2] twice (row max, then P = 2^(s - m) as fp16 into the P columns,
-//     each key half once the previous PV MMAs reading that half are done),
-//     rescales O when the row max moved; after a tile's last scores it writes
-//     the next tile's Q, then stores this tile's O;
+//     S[jg%2] twice (row max, then P = 2^(s - m) as fp16 written over the scores
+//     it has read, so P is double-buffered with S and never waits for a PV),
+//     rescales O when the row max moved (then, and only then, after PV(jg-1));
+//     after a tile's last scores it writes the next tile's Q, then stores this
+//     tile's O;
 //   MMA warp (warp 12, one thread): issues QK(jg) into S[jg%2] once K(jg) is
 //     written (and, on a tile's first KV tile, its Q), then PV(jg-1), each key
 //     half as soon as its V half is written.
@@ -990,14 +991,17 @@ __device__ __forceinline__ int chunk_tile_of(int c, int k, int C, int n) {
 // barrier phases follow it, so the next tile's loads, dequantisation and first
 // QK overlap this tile's last softmax and its epilogue.  The MMA issue blocks
 // its thread for about the MMA's duration, which is why one warp does nothing
-// else.  TMEM: Q | P (A operands, fp16) | S0 | S1 | O (fp32).  Every wait is
-// bounded; a timeout in any role makes all of them leave their loops.
+// else.  TMEM: Q (A operand, fp16) | S0 / P0 | S1 / P1 | O (fp32): P(jg) lies over
+// S[jg%2], PV(jg) reads it there, and QK(jg+2), the next writer of S[jg%2], is
+// issued after PV(jg) by the same thread (the MMAs of one thread run in issue
+// order).  Every wait is bounded; a timeout in any role makes all of them leave
+// their loops.
 template <int FK, int FV, int D>
 __device__ __forceinline__ void chunk_cta(const AttnParams& p, int cta, int n_ctas, uint8_t* smem_raw,
                                           unsigned int* err) {
   using L = ChunkSmem<FK, FV, D>;
   constexpr uint32_t kTmemCols = 512;
-  constexpr uint32_t kQCol = 0, kPCol = 64, kSCol0 = 128, kSCol1 = 256, kOCol = 384;
+  constexpr uint32_t kQCol = 0, kSCol0 = 128, kSCol1 = 256, kOCol = 384;  // P(j) lies over S[j % 2]
   constexpr int kGroup = 128;          // threads per warp group
   constexpr int kBarSoftmax = 1, kBarK = 2, kBarV = 3;
 
@@ -1163,10 +1167,9 @@ __device__ __forceinline__ void chunk_cta(const AttnParams& p, int cta, int n_ct
         const bool none = m_new == -CUDART_INF_F;
         const float alpha = none ? 1.f : ex2(m_run - m_new);
         const float neg_m = none ? 0.f : -m_new;
-        // pass 2: P = 2^(s*scale - m) as fp16 into the P columns (keys 32c.. of
-        // chunk c), each key half once the PV(j-1) MMAs reading that half of
-        // P(j-1) are done; row sums in fp32.  The scale-and-shift and the sums run
-        // on fp32 pairs.
+        // pass 2: P = 2^(s*scale - m) as fp16, written over the tile's own scores
+        // (S is double-buffered, so P is too: nothing here waits for PV(j-1)); row sums
+        // in fp32.  The scale-and-shift and the sums run on fp32 pairs.
         const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(neg_m, neg_m);
         uint64_t sum_a = f2_pack(0.f, 0.f), sum_b = sum_a;
 #pragma unroll 1
@@ -1190,11 +1193,10 @@ __device__ __forceinline__ void chunk_cta(const AttnParams& p, int cta, int n_ct
             pk[e >> 1] = pack_f16x2(p0, p1);
             pk[(e >> 1) + 1] = pack_f16x2(p2, p3);
           }
-          if (jg > 0 && (c & 1) == 0) {
-            ok = mbar_wait(&pvh_done[c >> 1], (uint32_t)((jg - 1) & 1), err) && ok;
-            tc_fence_after();
-          }
-          tmem_st16(tmem + lane_base + kPCol + 16 * c, pk);
+          // P over the scores already read (words 16c.. of the row = columns 16c.. of
+          // S[st]; chunks up to c are read by now): PV(jg) reads P there, and QK(jg+2),
+          // the next writer of S[st], is issued after PV(jg) by the same thread
+          tmem_st16(s_col + 16 * c, pk);
         }
         float sum0, sum1, sum2, sum3;
         f2_unpack(sum_a, sum0, sum1);
@@ -1203,9 +1205,12 @@ __device__ __forceinline__ void chunk_cta(const AttnParams& p, int cta, int n_ct
         sum1 += sum3;
         l_run = l_run * alpha + (sum0 + sum1);
         m_run = m_new;
-        // the running O: PV(j-1) has finished with it (its last half was waited above)
+        // the running O, once PV(j-1) has finished with it; only a warp with a row whose
+        // maximum moved waits for that
         if (j > 0) {
           if (__any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+            ok = mbar_wait(&pv_done[(jg - 1) & 1], (uint32_t)(((jg - 1) >> 1) & 1), err) && ok;
+            tc_fence_after();
 #pragma unroll 1
             for (int ch = 0; ch < D / 32; ++ch) {
               tmem_ld32(tmem + lane_base + kOCol + 32 * ch, a);
@@ -1335,7 +1340,8 @@ __device__ __forceinline__ void chunk_cta(const AttnParams& p, int cta, int n_ct
           const int jg = jg0 + j, st = jg & 1;
           const uint32_t s_col = tmem + (st ? kSCol1 : kSCol0);
           ok = mbar_wait(&kdeq[st], (uint32_t)((jg >> 1) & 1), err) && ok;  // K(jg) written to buffer st
-          // S[st] is free: the softmax of KV tile jg-2 read it before PV(jg-2) was issued
+          // S[st] holds P(jg-2), which PV(jg-2) reads; this thread issued PV(jg-2) before,
+          // and the MMAs of one thread run in issue order
           if (!ok) break;
           tc_fence_after();
           const uint32_t kd = st ? dK1 : dK0;  // low descriptor word of K buffer st
@@ -1351,7 +1357,7 @@ __device__ __forceinline__ void chunk_cta(const AttnParams& p, int cta, int n_ct
         if (j > 0) {
           const int jp = jg0 + j - 1, sp = jp & 1;
           ok = mbar_wait(&sm_done[sp], (uint32_t)((jp >> 1) & 1), err) && ok;  // P(jp) written, O rescaled
-          const uint32_t p_col = tmem + kPCol;
+          const uint32_t p_col = tmem + (sp ? kSCol1 : kSCol0);  // P(jp) lies over S(jp)
 #pragma unroll
           for (int hv = 0; hv < 2; ++hv) {
             ok = mbar_wait(&vdeq[hv], (uint32_t)(jp & 1), err) && ok;  // V half hv of KV tile jp written

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import workloads as wl
-from _harness import TOL, build_cache
+from _harness import TOL, build_cache, oracle_attention
 
 pytestmark = pytest.mark.gpu
 
@@ -51,6 +51,8 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls_in_a_row():
         assert np.isfinite(got).all()
         assert np.abs(got.astype(np.float64) - ref).max() <= TOL
     assert mq.device_error(clear=True) == 0
+    # and against the CPU oracle itself, not only against the other entry point
+    assert np.abs(got.astype(np.float64) - oracle_attention(w)).max() <= TOL
 
 
 def test_noalloc_rejects_a_batch_beyond_its_scratch():
