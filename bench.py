@@ -556,8 +556,9 @@ def main():
         prep = oracle_prepare(w, sel)
         cores = cpu_cores()
         # each step is one bounded sample (~3 s of oracle work at the default stride):
-        # up to 2 untimed warm-up steps, then up to K timed steps within ~2 minutes
-        warm = min(args.warmup, 2)
+        # 3 to 10 untimed warm-up steps (W, bounded), then up to K timed steps within
+        # ~2 minutes
+        warm = max(3, min(args.warmup, 10))
         for _ in range(warm):
             oracle_time(w, sel, prep, cores)
         times = [oracle_time(w, sel, prep, cores)]
@@ -566,7 +567,8 @@ def main():
         secs = sum(times) / len(times)
         val = len(sel) / secs
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
-                "steps": len(times), "steps_requested": args.steps, "warmup": warm, "ms_per_step": secs * 1e3,
+                "steps": len(times), "steps_requested": args.steps, "warmup": warm,
+                "warmup_requested": args.warmup, "ms_per_step": secs * 1e3,
                 "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": w.name, "kv_format": f"K={wl.FMT_NAMES[w.k_fmt]},V={wl.FMT_NAMES[w.v_fmt]}"},
