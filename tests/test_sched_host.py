@@ -164,7 +164,7 @@ def test_mark_all_decoders_due_after_a_step_with_a_chunk():
     run_until(b, lambda bt: b.counts()["decoders"] == 3)  # a decode step serving all three
     b.complete()
     b.submit(10, 5, 10000, 5)
-    # every decoder was served this round: the first slice runs alone, then all are due again
+    # every decoder was served in this rotation: the first slice runs alone, then all are due again
     bt = b.next_batch()
     assert bt.kind == mq.STEP_PREFILL and bt.request_ids == [10]
     b.complete()
