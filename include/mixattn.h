@@ -173,8 +173,10 @@ int mixattn_kv_export_blocks(const mixattn_kv_cache* cache, int32_t which, const
  * tiles is cut into 2-4 pieces whose partial results merge by log-sum-exp
  * (a choice made from the row itself and the device's SM count).  Decode rows
  * are cut into (kv head, page range) split-K tiles whose size depends only on
- * the row's own length.  So a row's output bits do not depend on the rest of
- * the batch.
+ * the row's own length; a chunk row of at most 24 (query, head) rows (a
+ * speculative-verify pass: up to 6 draft tokens at G = 4) runs on such tiles too,
+ * each holding up to 8 (query, head) rows.  So a row's output bits do not depend
+ * on the rest of the batch.
  *
  *   num_q_heads      multiple of cache->num_kv_heads; G = num_q_heads /
  *                    num_kv_heads must be 1, 2, 4 or 8

@@ -30,8 +30,10 @@ constexpr int kChunkN = 128;       // keys per KV tile of the chunk path (4 page
 constexpr int kPagesPerKvTile = kChunkN / kPage;
 constexpr int kMaxGroup = 8;       // q heads per kv head held in one mma N=8 tile
 constexpr int kMaxDevices = 64;    // per-device caches of the host side (device ordinals below this)
-constexpr int kVerifyMaxRows = 64; // a chunk row with q_len * G <= this (speculative verify) runs on
-                                   // decode-style split-K tiles of up to 8 (query, head) rows
+constexpr int kVerifyMaxRows = 24; // a chunk row with q_len * G <= this (speculative verify) runs on
+                                   // decode-style split-K tiles of up to 8 (query, head) rows: each
+                                   // such group costs about a third of a 128-row tensor-core tile
+                                   // per key, so up to three groups are cheaper than one tile
 
 // Per-row data the kernel needs (copied with the tile list).
 struct RowInfo {
