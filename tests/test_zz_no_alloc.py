@@ -36,9 +36,12 @@ def _call_noalloc(mq, cache, q, pt_d, w):
 def test_noalloc_matches_the_workspace_entry_point_on_two_calls_in_a_row():
     import torch
     import mixed_attention_quantized_gb300 as mq
-    # several decode rows with many split tiles (so the split counters matter) plus chunk rows
+    # several decode rows with many split tiles (so the split counters matter) plus chunk
+    # rows, one of them a 5-token verify-style row (verify groups on the workspace path, a
+    # tensor-core tile here)
     w = wl.custom("noalloc", 32, 8, 128, wl.FMT_Q8_0, wl.FMT_Q8_0, seed=41,
-                  rows=[(D, 9000, 8999), (C, 300, 100), (D, 33, 32), (D, 20000, 19999), (C, 64, 0)])
+                  rows=[(D, 9000, 8999), (C, 300, 100), (D, 33, 32), (D, 20000, 19999), (C, 64, 0),
+                        (C, 5005, 5000)])
     cache, pt = build_cache(w)
     q = torch.from_numpy(wl.queries(w)).cuda()
     pt_d = torch.from_numpy(pt).cuda()
